@@ -1,0 +1,152 @@
+// Fused argmax + greedy acceptance.
+// Source: "Laguna XS 2.1 33B on a RTX 3090" (lucebox), "The model, fast MoE with a drafter in the
+// box" (commit only tokens the target itself would emit) and "The Death of the Compute-Moat ...",
+// "DFlash Drafters and the End of Speculative Loss" (verify, commit, fall back to the target's
+// own token when no draft survives).
+//
+// Phase 1 (every CTA): a vocabulary segment of one logit row is scanned with 16-byte loads and
+// reduced to one 64-bit key per row, combined across CTAs with atomicMax. The key orders a row's
+// entries exactly like the greedy rule: high 32 bits = the fp32 value mapped to an unsigned
+// integer that sorts like the value (every NaN maps to the top, -0 to +0), low 32 bits = the
+// complement of the index (so equal values prefer the lower index).
+// Phase 2 (the last CTA to finish, by an atomic ticket; no CTA ever waits for another): decode
+// the argmax of every row, find each sequence's first draft mismatch with a warp ballot, write
+// the accepted length, the bonus token and the committed tokens, then zero the keys and the
+// ticket for the next call.
+#include "ptx.cuh"
+#include "vfy_internal.cuh"
+
+namespace vfy {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0xffffffffu;  // NaN: above everything
+  if (u == 0x80000000u) u = 0u;                              // -0 ties +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long pack(float x, int idx) {
+  return (static_cast<unsigned long long>(order_key(x)) << 32) |
+         static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ int unpack_index(unsigned long long key) {
+  return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull));
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) {
+  __shared__ unsigned long long warp_best[kThreads / 32];
+  __shared__ bool is_last;
+  pdl_wait();
+  const int row = blockIdx.y;
+  const int total_rows = p.cu_rows[p.num_seqs];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  if (row < total_rows && row < p.max_rows) {
+    const int v0 = blockIdx.x * p.seg;
+    const int v1 = min(p.vocab, v0 + p.seg);
+    const float* src = p.logits + static_cast<size_t>(row) * p.vocab;
+    unsigned long long best = 0ull;
+    if (VEC4) {
+      // v0 and the row start are multiples of 4 floats (16 bytes).
+      const float4* s4 = reinterpret_cast<const float4*>(src + v0);
+      const int n4 = v1 > v0 ? (v1 - v0) >> 2 : 0;
+      for (int i = threadIdx.x; i < n4; i += kThreads) {
+        const float4 v = __ldcs(s4 + i);
+        const int base = v0 + 4 * i;
+        const unsigned long long k01 = umax64(pack(v.x, base), pack(v.y, base + 1));
+        const unsigned long long k23 = umax64(pack(v.z, base + 2), pack(v.w, base + 3));
+        best = umax64(best, umax64(k01, k23));
+      }
+      for (int i = v0 + 4 * n4 + threadIdx.x; i < v1; i += kThreads) best = umax64(best, pack(src[i], i));
+    } else {
+      for (int i = v0 + threadIdx.x; i < v1; i += kThreads) best = umax64(best, pack(src[i], i));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+    if (lane == 0) warp_best[warp] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long b = warp_best[0];
+      for (int w = 1; w < kThreads / 32; ++w) b = umax64(b, warp_best[w]);
+      atomicMax(p.keys + row, b);
+    }
+  } else if (threadIdx.x == 0 && row == 0 && blockIdx.x == 0 && total_rows > p.max_rows) {
+    atomicOr(p.err, kErrDeviceInput);
+  }
+
+  // Ticket: the last CTA of the grid does the acceptance.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int total = gridDim.x * gridDim.y;
+    const unsigned int ticket = atomicAdd(p.counter, 1u);
+    is_last = (ticket == total - 1);
+  }
+  __syncthreads();
+  if (!is_last) {
+    pdl_launch_dependents();
+    return;
+  }
+  __threadfence();
+
+  const int rows_done = min(total_rows, p.max_rows);
+  for (int b = warp; b < p.num_seqs; b += kThreads / 32) {
+    const int r0 = p.cu_rows[b];
+    const int r1 = p.cu_rows[b + 1];
+    const int depth = r1 - r0 - 1;
+    if (r0 < 0 || depth < 0 || r1 > rows_done) {
+      if (lane == 0) atomicOr(p.err, kErrDeviceInput);
+      continue;
+    }
+    const int d0 = r0 - b;   // drafts of sequence b start after the D_b' of earlier sequences
+    int n = depth;
+    for (int j0 = 0; j0 < depth; j0 += 32) {
+      const int j = j0 + lane;
+      bool mismatch = false;
+      if (j < depth) {
+        const int a = unpack_index(__ldcg(p.keys + r0 + j));
+        mismatch = a != p.drafts[d0 + j];
+      }
+      const unsigned ballot = __ballot_sync(0xffffffffu, mismatch);
+      if (ballot != 0u) {
+        n = j0 + __ffs(ballot) - 1;
+        break;
+      }
+    }
+    const int bonus = unpack_index(__ldcg(p.keys + r0 + n));
+    for (int j = lane; j <= depth; j += 32) {
+      int tok = -1;
+      if (j < n) tok = p.drafts[d0 + j];
+      else if (j == n) tok = bonus;
+      p.committed[r0 + j] = tok;
+    }
+    if (lane == 0) {
+      p.accepted_len[b] = n;
+      p.bonus[b] = bonus;
+    }
+  }
+  __syncthreads();
+  // Leave the workspace as this call found it: all keys zero, ticket zero.
+  for (int r = threadIdx.x; r < p.max_rows; r += kThreads) p.keys[r] = 0ull;
+  if (threadIdx.x == 0) *p.counter = 0u;
+  __threadfence();
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_accept(const AcceptParams& p, bool vec4, cudaStream_t stream) {
+  dim3 grid(p.parts, p.max_rows);
+  if (vec4) return launch_pdl(accept_kernel<true>, grid, dim3(kThreads), 0, stream, p);
+  return launch_pdl(accept_kernel<false>, grid, dim3(kThreads), 0, stream, p);
+}
+
+}  // namespace vfy

@@ -1,0 +1,555 @@
+// Verify attention on sm_103a: split-KV flash-decode with TMA-staged bf16 K/V tiles, tcgen05
+// tensor-core tiles for S = Q K^T and O += P V (fp32 accumulators in tensor memory), an fp32
+// online softmax, and a warp-shuffle combine of the splits.
+//
+// Sources ("Laguna XS 2.1 33B on a RTX 3090" (lucebox)):
+//  - "The model, fast MoE with a drafter in the box": the 16 drafted tokens and the last committed
+//    token are verified in one batched target forward. Here the q = D + 1 block queries of one
+//    KV head's G q-heads form q * G <= 128 rows, the M = 128 side of one tcgen05 MMA.
+//  - "Three optimizations", item 1: full layers read a pool of 64-token chunks, of which a resident
+//    subset is on the GPU. Each resident chunk is one 64-token tile, fetched by TMA from its slot.
+//  - item 3: window layers attend a 512-token window kept in a 2048-slot position ring. The ring
+//    tiles are 64-slot aligned, so a tile never crosses the ring's end.
+//
+// One CTA handles one (sequence b, KV head h, split s): a contiguous run of tiles. Warp roles:
+//   warps 0-3  load Q, then one thread per TMEM lane / row: masked online softmax, epilogue
+//   warp 4     TMA producer (K and V tiles into a ring of smem stages)
+//   warp 5     TMEM owner and MMA issuer (one elected lane)
+// Row r = i * G + g (query i, q-head g of the group) sits in TMEM lane (r % 4) * 32 + r / 4, so the
+// real rows spread over the four lane quarters and all four softmax warps share the work.
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "vfy_internal.cuh"
+
+namespace vfy {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;     // O accumulator: d columns
+constexpr uint32_t kColS = 128;   // two S buffers of 64 columns
+constexpr uint32_t kColP = 256;   // two P buffers of 32 columns (64 bf16 packed in pairs)
+// A row keeps a stale reference maximum until a tile's maximum exceeds it by this much (log2
+// units); then O and l are rescaled. The result is exact either way: O and l share the reference.
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int HD>
+struct Cfg {
+  static constexpr int kBoxes = HD / 64;               // 128-byte (64-column) boxes per row
+  static constexpr int kBoxBytes = kChunk * 128;       // one 64-row box
+  static constexpr int kQBoxBytes = kMaxRows * 128;
+  static constexpr int kQBytes = kMaxRows * HD * 2;
+  static constexpr int kTileBytes = kChunk * HD * 2;
+  static constexpr int kStages = HD == 128 ? 5 : 8;
+  static constexpr int kBarOffset = kQBytes + 2 * kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOffset + 1024 + 1024;
+};
+
+struct Bars {
+  uint64_t k_full[8];
+  uint64_t v_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full;
+  uint64_t q_ready;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// The per-CTA work item.
+struct Work {
+  int b, h, s;
+  int q0, nq, rows;
+  int L;
+  int tb, nt;      // first tile (index within the (b, h) tile list) and number of tiles
+  int r0;          // full: resident-list offset of sequence b
+  int lo, span;    // ring: first attended position of the block and the union span length
+  int s_lo;        // ring: slot of position lo
+  bool bad;        // the sequence's q or L is out of range: it is skipped
+};
+
+template <bool RING>
+__device__ __forceinline__ Work make_work(const AttnParams& p) {
+  Work w;
+  w.b = blockIdx.z;
+  w.h = blockIdx.y;
+  w.s = blockIdx.x;
+  w.q0 = p.cu_q[w.b];
+  w.nq = p.cu_q[w.b + 1] - w.q0;
+  w.L = p.seq_len[w.b];
+  w.tb = 0;
+  w.nt = 0;
+  w.r0 = 0;
+  w.lo = 0;
+  w.span = 0;
+  w.s_lo = 0;
+  w.bad = w.nq < 0 || w.nq > p.max_q || w.L < w.nq || w.q0 < 0;
+  if (w.bad) {
+    w.nq = 0;
+    w.rows = 0;
+    return w;
+  }
+  w.rows = w.nq * p.group;
+  int n_tiles;
+  if (!RING) {
+    w.r0 = p.cu_res[w.b];
+    n_tiles = p.cu_res[w.b + 1] - w.r0;
+    if (n_tiles < 0) n_tiles = 0;
+  } else {
+    const int R = p.ring_len;
+    int phi = p.ring_off[w.b];
+    phi = ((phi % R) + R) % R;
+    w.lo = max(0, w.L - w.nq - p.window + 1);
+    w.span = w.L - w.lo;
+    w.s_lo = static_cast<int>((static_cast<long long>(w.lo) + phi) % R);
+    n_tiles = w.span > 0 ? ((w.s_lo & (kChunk - 1)) + w.span + kChunk - 1) / kChunk : 0;
+  }
+  const long long ns = p.num_splits;
+  w.tb = static_cast<int>((static_cast<long long>(w.s) * n_tiles) / ns);
+  w.nt = static_cast<int>((static_cast<long long>(w.s + 1) * n_tiles) / ns) - w.tb;
+  return w;
+}
+
+// Tile geometry: the TMA row coordinate of the tile's first token, and what the mask needs.
+struct Tile {
+  int y;          // row of the 2-D [rows][d] view of the pool / ring
+  int base;       // full: position of token 0; ring: offset (from s_lo, mod R) of slot 0
+  bool valid;     // full: slot and chunk id in range
+};
+
+template <bool RING>
+__device__ __forceinline__ Tile tile_at(const AttnParams& p, const Work& w, int j) {
+  Tile t;
+  if (!RING) {
+    const int idx = w.r0 + w.tb + j;
+    const int cid = p.res_ids[idx];
+    const int slot = p.res_slots[idx];
+    t.valid = cid >= 0 && cid < (1 << 25) && slot >= 0 && slot < p.num_slots;
+    t.y = (t.valid ? (slot * p.hkv + w.h) : w.h) * kChunk;
+    t.base = t.valid ? cid * kChunk : 0;
+  } else {
+    const int R = p.ring_len;
+    const int tiles_per_ring = R / kChunk;
+    const int ti = (w.s_lo / kChunk + w.tb + j) % tiles_per_ring;
+    t.valid = true;
+    t.y = ((w.b * p.hkv + w.h) * R) + ti * kChunk;
+    t.base = ((ti * kChunk - w.s_lo) % R + R) % R;
+  }
+  return t;
+}
+
+// Is key k of the tile at a position some block query attends (inside the union span)?
+template <bool RING>
+__device__ __forceinline__ bool key_in_union(const AttnParams& p, const Work& w, const Tile& t, int k,
+                                             int* pos_out) {
+  if (!RING) {
+    const int pos = t.base + k;
+    *pos_out = pos;
+    return t.valid && pos < w.L;
+  } else {
+    int off = t.base + k;
+    if (off >= p.ring_len) off -= p.ring_len;
+    *pos_out = w.lo + off;
+    return off < w.span;
+  }
+}
+
+template <int HD, bool RING>
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v) {
+  using C = Cfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + C::kQBytes;
+  uint8_t* sV = sK + C::kStages * C::kTileBytes;
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOffset);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- prologue (overlaps the previous kernel under programmatic dependent launch) ----------
+  if (threadIdx.x == 128) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 128);
+    }
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+
+  pdl_wait();
+  const Work w = make_work<RING>(p);
+  if (w.bad && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, kErrDeviceInput);
+
+  const uint32_t idesc_s = idesc_bf16_f32(128, kChunk, 0, 0);
+  const uint32_t idesc_pv = idesc_bf16_f32(128, HD, 0, 1);
+  const size_t pidx = (static_cast<size_t>(w.b) * p.hkv + w.h) * p.num_splits + w.s;
+
+  if (warp == 4) {
+    // ------------------------------ TMA producer -----------------------------------------
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int issued = 0;
+      bool reported = false;
+      for (int j = 0; j < w.nt; ++j) {
+        const int st = j % C::kStages;
+        if (j >= C::kStages && !mbar_wait(&bars->kv_empty[st], ((j / C::kStages) - 1) & 1, abort, p.err)) break;
+        const Tile t = tile_at<RING>(p, w, j);
+        if (!t.valid && !reported) {
+          atomicOr(p.err, kErrDeviceInput);
+          reported = true;
+        }
+        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &tmap_k, &bars->k_full[st], bx * 64, t.y, pol);
+        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &tmap_v, &bars->v_full[st], bx * 64, t.y, pol);
+        issued = j + 1;
+      }
+      if (*abort) {
+        // Let every copy still in flight land before the CTA can exit.
+        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+          mbar_drain(&bars->k_full[j % C::kStages], (j / C::kStages) & 1);
+          mbar_drain(&bars->v_full[j % C::kStages], (j / C::kStages) & 1);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------ MMA issuer -------------------------------------------
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_ready, 0, abort, p.err));
+    tc_fence_after();
+    const uint32_t qaddr = smem_u32(sQ);
+    for (int j = 0; ok && j <= w.nt; ++j) {
+      if (j < w.nt) {
+        // S_j = Q K_j^T into S buffer j % 2
+        const int st = j % C::kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (j / C::kStages) & 1, abort, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t kaddr = smem_u32(sK + st * C::kTileBytes);
+          const uint32_t d_s = tbase + kColS + (j & 1) * 64;
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint64_t a = sw128_desc(qaddr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t bdesc = sw128_desc(kaddr + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+            mma_ss(d_s, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[j & 1]);
+        }
+        __syncwarp();
+      }
+      if (j >= 1) {
+        // O += P_{j-1} V_{j-1}
+        const int jp = j - 1;
+        const int st = jp % C::kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_full[jp & 1], (jp >> 1) & 1, abort, p.err));
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (jp / C::kStages) & 1, abort, p.err));
+        if (!ok) break;
+        // Keys outside every query's range may hold anything (stale ring slots, the unused tail
+        // of the last chunk). P is 0 there, but 0 * NaN is NaN on the tensor core, so their V rows
+        // are zeroed before the MMA reads them.
+        {
+          const Tile t = tile_at<RING>(p, w, jp);
+          uint8_t* vt = sV + st * C::kTileBytes;
+          bool any = false;
+          for (int k = lane; k < kChunk; k += 32) {
+            int pos;
+            if (!key_in_union<RING>(p, w, t, k, &pos)) {
+              any = true;
+#pragma unroll
+              for (int bx = 0; bx < C::kBoxes; ++bx) {
+                uint4* row = reinterpret_cast<uint4*>(vt + bx * C::kBoxBytes + k * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+          }
+          if (any) fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vaddr = smem_u32(sV + st * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kChunk / 16; ++kk) {
+            const uint64_t bdesc = sw128_desc(vaddr + kk * 2048, C::kBoxBytes, 1024);
+            mma_ts(tbase + kColO, tbase + kColP + (jp & 1) * 32 + kk * 8, bdesc, idesc_pv,
+                   (jp > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->kv_empty[st]);
+          mma_commit(&bars->o_full);
+        }
+        __syncwarp();
+      }
+    }
+    // Every MMA issued above completes before TMEM is freed.
+    if (lane == 0) mma_commit(&bars->drain);
+    __syncwarp();
+    mbar_drain(&bars->drain, 0);
+  } else {
+    // ------------------------------ softmax / epilogue (warps 0-3) ------------------------
+    const int mrow = threadIdx.x;                      // TMEM lane and Q smem row
+    const int r = (mrow & 31) * 4 + (mrow >> 5);        // block row held by this lane
+    const bool rv = r < w.rows;
+    const int qi = rv ? r / p.group : 0;
+    const int g = rv ? r % p.group : 0;
+    // Q row -> swizzled smem (the 128-byte swizzle TMA would apply: chunk c of row m at c ^ (m & 7)).
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<size_t>(w.q0 + qi) * p.hq + static_cast<size_t>(w.h) * p.group + g) * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 8; ++c) {
+        const uint4 v = rv ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        const int bx = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(sQ + bx * C::kQBoxBytes + mrow * 128 + ((cc ^ (mrow & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->q_ready);
+    }
+    const int p_i = w.L - w.nq + qi;                   // this row's query position
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    float m_ref = -INFINITY;
+    float l_sum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < w.nt; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s_lo[32], s_hi[32];
+      tmem_ld32(lane_base + kColS + (j & 1) * 64, s_lo);
+      tmem_ld32(lane_base + kColS + (j & 1) * 64 + 32, s_hi);
+      const Tile t = tile_at<RING>(p, w, j);
+      float x[64];
+      float m_tile = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        int pos;
+        bool v = key_in_union<RING>(p, w, t, k, &pos) && rv && pos <= p_i;
+        if (RING) v = v && pos > p_i - p.window;
+        const uint32_t bits = k < 32 ? s_lo[k] : s_hi[k - 32];
+        x[k] = v ? __uint_as_float(bits) * p.scale_log2 : -INFINITY;
+        m_tile = fmaxf(m_tile, x[k]);
+      }
+      bool need_o = false;
+      float alpha = 1.f;
+      if (m_tile > m_ref + kRescaleLog2) {
+        alpha = ex2_approx(m_ref - m_tile);           // 0 when m_ref = -inf
+        need_o = l_sum > 0.f;
+        l_sum *= alpha;
+        m_ref = m_tile;
+      }
+      if (__any_sync(0xffffffffu, need_o)) {
+        // O holds the sum over tiles < j: wait for PV_{j-1}, then scale the rows that need it.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full, (j - 1) & 1, abort, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        const float a = need_o ? alpha : 1.f;
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kColO + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+          tmem_st32(lane_base + kColO + c * 32, o);
+        }
+      }
+      uint32_t pk[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = x[2 * e] == -INFINITY ? 0.f : ex2_approx(x[2 * e] - m_ref);
+        const float p1 = x[2 * e + 1] == -INFINITY ? 0.f : ex2_approx(x[2 * e + 1] - m_ref);
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+        psum += __low2float(h2) + __high2float(h2);
+        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      l_sum += psum;
+      tmem_st32(lane_base + kColP + (j & 1) * 32, pk);
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[j & 1]);
+    }
+    // ---- epilogue: the split's partial (m, l, unnormalised O) ----
+    if (ok && w.nt > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full, (w.nt - 1) & 1, abort, p.err));
+      tc_fence_after();
+    }
+    if (ok) {
+      float* dst = p.part_o + (pidx * kMaxRows + r) * HD;
+      if (w.nt > 0) {
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kColO + c * 32, o);
+          if (rv && l_sum > 0.f) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + c * 32 + e) =
+                  make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
+                              __uint_as_float(o[e + 3]));
+          }
+        }
+      }
+      if (rv) {
+        float2* ml = reinterpret_cast<float2*>(p.part_ml) + pidx * kMaxRows + r;
+        *ml = make_float2(l_sum > 0.f ? m_ref : -INFINITY, l_sum);
+      }
+    }
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ------------------------------ split combine ---------------------------------------------------
+// One warp per output row (token t, q-head hq). Lanes first reduce the splits' maxima with
+// shuffles, then each lane accumulates HD/32 columns of sum_s 2^(m_s - M) o_s and the weights.
+//   O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  LSE = ln2 * (M + log2 sum_s 2^(m_s - M) l_s)
+template <int HD>
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int t = static_cast<int>(row / p.hq);
+  const int hq = static_cast<int>(row % p.hq);
+  if (t >= p.token_cap) return;
+  const int total = p.cu_q[p.num_seqs];
+  if (t >= total) return;
+  int b = 0;
+  while (b + 1 < p.num_seqs && p.cu_q[b + 1] <= t) ++b;
+  const int i = t - p.cu_q[b];
+  const int nq = p.cu_q[b + 1] - p.cu_q[b];
+  if (i < 0 || nq < 0 || nq > p.max_q || p.seq_len[b] < nq) return;   // skipped by the attention kernel too
+  const int h = hq / p.group;
+  const int r = i * p.group + hq % p.group;
+  const size_t p0 = (static_cast<size_t>(b) * p.hkv + h) * p.num_splits;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+
+  float mmax = -INFINITY;
+  for (int s = lane; s < p.num_splits; s += 32) {
+    const float2 v = ml[(p0 + s) * kMaxRows + r];
+    if (v.y > 0.f) mmax = fmaxf(mmax, v.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+
+  constexpr int kPer = HD / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float lsum = 0.f;
+  if (mmax != -INFINITY) {
+    for (int s0 = 0; s0 < p.num_splits; s0 += 32) {
+      const int s = s0 + lane;
+      float wgt = 0.f, lw = 0.f;
+      if (s < p.num_splits) {
+        const float2 v = ml[(p0 + s) * kMaxRows + r];
+        if (v.y > 0.f) {
+          wgt = ex2_approx(v.x - mmax);
+          lw = wgt * v.y;
+        }
+      }
+      lsum += lw;
+      const int cnt = min(32, p.num_splits - s0);
+      for (int k = 0; k < cnt; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, wgt, k);
+        if (wk == 0.f) continue;   // never read a split that holds no row data
+        const float* src = p.part_o + ((p0 + s0 + k) * kMaxRows + r) * HD + lane * kPer;
+        if constexpr (kPer == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] += wk * v.x;
+          acc[1] += wk * v.y;
+          acc[2] += wk * v.z;
+          acc[3] += wk * v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          acc[0] += wk * v.x;
+          acc[1] += wk * v.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  uint16_t* dst = p.out + (static_cast<size_t>(t) * p.hq + hq) * HD + lane * kPer;
+  if constexpr (kPer == 4) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    const __nv_bfloat162 c = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&a);
+    v.y = *reinterpret_cast<const uint32_t*>(&c);
+    *reinterpret_cast<uint2*>(dst) = v;
+  } else {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&a);
+  }
+  if (p.lse != nullptr && lane == 0) {
+    p.lse[static_cast<size_t>(t) * p.hq + hq] =
+        lsum > 0.f ? (mmax + __log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+  }
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+template <int HD, bool RING>
+static cudaError_t launch_attend_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   int num_seqs, cudaStream_t stream) {
+  static size_t done[64] = {};
+  auto kern = attend_kernel<HD, RING>;
+  cudaError_t e = ensure_smem_limit(kern, Cfg<HD>::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.num_splits, p.hkv, num_seqs);
+  return launch_pdl(kern, grid, dim3(kThreads), Cfg<HD>::kSmemBytes, stream, p, tk, tv);
+}
+
+cudaError_t launch_attend(bool ring, int head_dim, const AttnParams& p, const CUtensorMap& tk,
+                          const CUtensorMap& tv, int num_seqs, cudaStream_t stream) {
+  if (head_dim == 128)
+    return ring ? launch_attend_t<128, true>(p, tk, tv, num_seqs, stream)
+                : launch_attend_t<128, false>(p, tk, tv, num_seqs, stream);
+  return ring ? launch_attend_t<64, true>(p, tk, tv, num_seqs, stream)
+              : launch_attend_t<64, false>(p, tk, tv, num_seqs, stream);
+}
+
+cudaError_t launch_combine(int head_dim, const CombineParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.token_cap) * p.hq;
+  dim3 grid(static_cast<unsigned>((rows + 3) / 4));
+  if (head_dim == 128) return launch_pdl(combine_kernel<128>, grid, dim3(128), 0, stream, p);
+  return launch_pdl(combine_kernel<64>, grid, dim3(128), 0, stream, p);
+}
+
+}  // namespace vfy

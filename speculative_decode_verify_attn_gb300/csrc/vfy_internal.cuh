@@ -1,0 +1,146 @@
+// Internal declarations shared by the host API (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <utility>
+
+#include "../../include/vfy.h"
+
+namespace vfy {
+
+constexpr int kChunk = 64;          // tokens per pool chunk and per attention tile
+constexpr int kMaxRows = 128;       // q * G rows of one (sequence, KV head) in the M = 128 MMA
+constexpr int kMaxSelectChunks = 32768;
+constexpr int kMaxSelectK = 4096;
+
+// ------------------------------ attention ---------------------------------------------------
+struct AttnParams {
+  const uint16_t* q;          // [T][Hq][d]
+  const int32_t* cu_q;        // [B+1]
+  const int32_t* seq_len;     // [B]
+  // full layers: resident list
+  const int32_t* res_ids;
+  const int32_t* res_slots;
+  const int32_t* cu_res;
+  int num_slots;
+  // window layers: ring
+  const int32_t* ring_off;    // [B]
+  int ring_len;
+  int window;
+  // shapes
+  int hq, hkv, group;
+  int num_splits;
+  int max_q;
+  float scale_log2;           // softmax scale * log2(e)
+  // split partials (workspace)
+  float* part_o;              // [B][Hkv][splits][128][d]
+  float* part_ml;             // [B][Hkv][splits][128][2] (m in log2 units, l)
+  int* err;
+};
+
+struct CombineParams {
+  const int32_t* cu_q;
+  const int32_t* seq_len;
+  int num_seqs;
+  int hq, hkv, group;
+  int num_splits;
+  int max_q;
+  int token_cap;              // host bound on cu_q[B]
+  const float* part_o;
+  const float* part_ml;
+  uint16_t* out;              // [T][Hq][d]
+  float* lse;                 // [T][Hq] or null
+  int* err;
+};
+
+cudaError_t launch_attend(bool ring, int head_dim, const AttnParams& p, const CUtensorMap& tk,
+                          const CUtensorMap& tv, int num_seqs, cudaStream_t stream);
+cudaError_t launch_combine(int head_dim, const CombineParams& p, cudaStream_t stream);
+
+// ------------------------------ acceptance --------------------------------------------------
+struct AcceptParams {
+  const float* logits;
+  int vocab;
+  const int32_t* drafts;
+  const int32_t* cu_rows;
+  int num_seqs;
+  int max_rows;
+  int parts;                  // CTAs per row
+  int seg;                    // vocab entries per CTA (multiple of 4)
+  int32_t* accepted_len;
+  int32_t* bonus;
+  int32_t* committed;
+  unsigned long long* keys;   // [max_rows] workspace, zero between calls
+  unsigned int* counter;      // workspace, zero between calls
+  int* err;
+};
+cudaError_t launch_accept(const AcceptParams& p, bool vec4, cudaStream_t stream);
+
+// ------------------------------ residency ---------------------------------------------------
+struct SelectParams {
+  const float* scores;
+  const int32_t* cu_chunks;
+  int num_seqs;
+  int max_n;
+  int k;
+  int32_t* slot_of_chunk;
+  int32_t* res_ids;
+  int32_t* res_slots;
+  int32_t* cu_res;
+  int32_t* pagein_list;
+  int32_t* pagein_count;
+  int* err;
+};
+cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
+
+struct PageInParams {
+  const uint16_t* host_k;
+  const uint16_t* host_v;
+  long long num_host_chunks;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  int num_slots;
+  const int32_t* list;
+  const int32_t* count;
+  int num_seqs;
+  int k;
+  long long chunk_elems;      // Hkv * 64 * d
+  int* err;
+};
+cudaError_t launch_page_in(const PageInParams& p, cudaStream_t stream);
+
+// Launch with the programmatic-stream-serialization attribute so that a kernel's prologue can
+// overlap the tail of the kernel before it; every kernel calls griddepcontrol.wait before it
+// touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Sets the dynamic shared-memory limit of `kernel` once per device (the attribute is per device).
+template <typename K>
+cudaError_t ensure_smem_limit(K kernel, size_t bytes, size_t* done_per_device) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done_per_device[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done_per_device[dev] = bytes;
+  return e;
+}
+
+}  // namespace vfy
