@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verify pass on GB300.
+
+Workload: one verify step at 256K context with a 16-token draft, the 40-layer pass of the
+Laguna XS 2.1 shape (16 q-heads / 4 KV heads x 128; 30 window layers over a 2048-slot ring,
+10 full layers over an 8K-token resident pool of 4096 64-token chunks, 16 chunks paged in from
+pinned host memory per step; greedy acceptance over 17 x 131072 fp32 logits at a 56% draft match
+rate), captured once as a CUDA graph and replayed. Inputs are synthetic and seeded.
+
+One JSON line on stdout (rank 0):
+  metric/unit   verify-attention microseconds per layer (lower is better), whole pass / 40 layers,
+                KV GB/s and the fraction of measured HBM bandwidth reported beside it
+  value         device time of the graph replay, L2 flushed (256 MiB write) between steps
+  e2e           the same, with the step's inputs copied host->device from pinned memory and the
+                accepted tokens copied back inside the timed region
+  roofline      for the dominant kernel (full-layer attention): algorithmic bytes / event time
+  cpu_baseline  the fp64 CPU oracle on a bounded sample, one host core
+Multi-GPU (torchrun): replicas only, one pass per GPU, no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn µs/layer and KV GB/s (% of HBM peak) at 256K ctx, 16-token draft"
+UNIT = "us/layer"
+FLUSH_BYTES = 256 << 20
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the all-resident and per-kernel points")
+    ap.add_argument("--oracle-sample", type=float, default=0.0, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------------------------
+# Distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------------------------
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def dist_setup(backend):
+    import torch.distributed as dist
+    rank, local, world = dist_info()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def dist_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate_us_per_layer(ms_per_step_max: float, layers: int, n_gpus: int) -> float:
+    """Whole-job time per layer: all ranks' layers in the slowest rank's time."""
+    return ms_per_step_max * 1000.0 / (layers * n_gpus)
+
+
+# ---------------------------------------------------------------------------------------------
+# Clocks
+# ---------------------------------------------------------------------------------------------
+
+def start_clock_sampler(device_index: int, path: str):
+    import torch
+    ident = str(device_index)
+    try:
+        uuid = torch.cuda.get_device_properties(device_index).uuid
+        ident = "GPU-" + str(uuid)
+    except Exception:
+        pass
+    try:
+        f = open(path, "w")
+        return subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                 "-lms", "100", "-i", ident], stdout=f, stderr=subprocess.DEVNULL), f
+    except Exception:
+        return None, None
+
+
+def stop_clock_sampler(proc, f, path):
+    if proc is None:
+        return None
+    proc.terminate()
+    try:
+        proc.wait(timeout=5)
+    except Exception:
+        proc.kill()
+    f.close()
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in open(path):
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[5:9]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# Peaks
+# ---------------------------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle sample (one host core)
+# ---------------------------------------------------------------------------------------------
+
+def oracle_sample_seconds(budget_s: float) -> dict:
+    """Time the fp64 oracle on one full layer (8K resident of 4096 chunks), one window layer,
+    the residency selection, 16 page-ins and the acceptance, repeated for about budget_s; scale
+    to the 40-layer pass (10 full + 30 window)."""
+    import numpy as np
+
+    from oracle import vfy_oracle as O
+    from speculative_decode_verify_attn_gb300 import synth
+
+    rng = np.random.default_rng(0)
+    s = synth.LAGUNA
+    L, q, n, k = 262144, 17, 4096, 128
+    rot = synth.rotating_residency(rng, n, k, 16, L, q)
+    scores = rot.scores(1)
+    prev = np.full(n, -1)
+    res0 = O.select_resident(rot.scores(0), [0, n], k, prev)
+    pool_k = synth.normal_bf16(rng, (k, s.num_kv_heads, 64, s.head_dim))
+    pool_v = synth.normal_bf16(rng, (k, s.num_kv_heads, 64, s.head_dim))
+    host_k = synth.normal_bf16(rng, (32, s.num_kv_heads, 64, s.head_dim))
+    host_v = synth.normal_bf16(rng, (32, s.num_kv_heads, 64, s.head_dim))
+    ring_k = synth.normal_bf16(rng, (s.num_kv_heads, synth.RING, s.head_dim))
+    ring_v = synth.normal_bf16(rng, (s.num_kv_heads, synth.RING, s.head_dim))
+    phi = synth.wrapping_ring_offset(rng, L, 512 + q - 1, synth.RING)
+    qb = synth.normal_bf16(rng, (q, s.num_q_heads, s.head_dim))
+    targets = rng.integers(0, synth.VOCAB, q)
+    logits = synth.planted_logits(rng, targets, synth.VOCAB)
+    drafts = synth.drafts_matching(rng, targets, 0.56, synth.VOCAB)
+    t = {"select": [], "page_in": [], "full": [], "swa": [], "accept": []}
+    t_end = time.perf_counter() + budget_s
+    reps = 0
+    while reps < 1 or time.perf_counter() < t_end:
+        a = time.perf_counter()
+        res = O.select_resident(scores, [0, n], k, res0["slot_of_chunk"])
+        b = time.perf_counter()
+        pairs = [(c % 32, s_) for c, s_ in res["pagein"][0]]
+        O.page_in(host_k, host_v, pool_k, pool_v, pairs)
+        c = time.perf_counter()
+        O.attend_full_seq(qb, pool_k, pool_v, res["resident_ids"], res["resident_slots"], L)
+        d = time.perf_counter()
+        O.attend_ring_seq(qb, ring_k, ring_v, phi, L, 512)
+        e = time.perf_counter()
+        O.accept(logits, drafts, [0, q])
+        f = time.perf_counter()
+        for key, dt in zip(t, (b - a, c - b, d - c, e - d, f - e)):
+            t[key].append(dt)
+        reps += 1
+    m = {key: statistics.mean(v) for key, v in t.items()}
+    pass_s = m["select"] + 10 * m["page_in"] + 10 * m["full"] + 30 * m["swa"] + m["accept"]
+    return {"us_per_layer": pass_s * 1e6 / 40, "reps": reps, "parts_s": m, "pass_s": pass_s}
+
+
+def run_oracle_child(budget_s: float) -> dict:
+    """Run the oracle sample in a child process pinned to one BLAS / OpenMP thread."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", str(budget_s)],
+                         capture_output=True, text=True, env=env, cwd=ROOT)
+    if out.returncode != 0:
+        raise RuntimeError("oracle sample failed:\n" + out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_obj(res: dict) -> dict:
+    return {"value": round(res["us_per_layer"], 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"fp64 numpy oracle, one thread: 1 full layer (128 of 4096 chunks resident, 17 queries x "
+                       f"16 heads), 1 window layer, residency top-128 of 4096, 16 page-ins, accept over 17 x 131072; "
+                       f"{res['reps']} repetitions, scaled to 10 full + 30 window layers per pass / 40")}
+
+
+# ---------------------------------------------------------------------------------------------
+# Reference arm: the oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, local, world = dist_info()
+    if rank != 0:
+        return 0
+    steps = max(1, min(args.steps, 40))
+    warm = min(args.warmup, 2)
+    for _ in range(warm):
+        run_oracle_child(0.0)
+    vals = []
+    t0 = time.perf_counter()
+    last = None
+    for _ in range(steps):
+        last = run_oracle_child(0.0)
+        vals.append(last["us_per_layer"])
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": round(value * 40 / 1000, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "verify pass, 256K context, 16-token draft (sampled on the CPU)",
+                       "steps_capped_at": 40, "wall_s": round(wall, 2)},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": cpu_baseline_obj(last)["sample"]},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------------------------
+
+def event_time_graph(graph, flush, steps, pre=None):
+    """Mean / median device time (ms) of graph replays, L2 flushed before each."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        if pre is not None:
+            pre(i)
+        flush.zero_()
+        starts[i].record()
+        graph.replay()
+        ends[i].record()
+    torch.cuda.synchronize()
+    ts = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return statistics.mean(ts), statistics.median(ts), ts
+
+
+def capture(fn):
+    import torch
+    fn()                      # eager once (sets kernel attributes outside capture)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def run_ours(args):
+    import torch
+
+    import __graft_entry__
+    from speculative_decode_verify_attn_gb300 import passes, synth
+
+    rank, local, world = dist_setup("nccl" if args.gpus > 1 else "gloo")
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    peak, peak_kind = hbm_peak()
+
+    wl = synth.workload_256k()
+    vp = passes.VerifyPass(wl, device=local, seed=rank)
+    sz = vp.sizes()
+    vp.capture()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    # warm-up: steady-state residency (16 new chunks per step)
+    for i in range(max(args.warmup, 3)):
+        vp.set_step_scores(vp.step)
+        vp.step += 1
+        flush.zero_()
+        vp.replay()
+    torch.cuda.synchronize()
+
+    def next_scores(i):
+        vp.set_step_scores(vp.step)
+        vp.step += 1
+
+    clk_path = os.path.join(tempfile.gettempdir(), f"vfy_clocks_{os.getpid()}.csv")
+    proc, fh = start_clock_sampler(local, clk_path)
+    time.sleep(0.3)
+    dist_barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    mean_ms, med_ms, ts = event_time_graph(vp.graph, flush, args.steps, pre=next_scores)
+    torch.cuda.synchronize()
+    dist_barrier()
+    wall = time.perf_counter() - wall0
+    clocks = stop_clock_sampler(proc, fh, clk_path)
+    ms_max = dist_max(mean_ms, torch.device("cuda", local))
+    accepted = int(vp.accepted.item())
+
+    launches = vp.launches_per_step() * args.steps
+    value = aggregate_us_per_layer(ms_max, sz.n_layers, world)
+    kv_gbs = sz.bytes_pass / (mean_ms * 1e-3) / 1e9
+
+    extras = {}
+    roofline = None
+    if not args.no_extras:
+        # per-kernel points: one full layer, one window layer, acceptance, select + page-in
+        lf, ls = vp.full_layers[0], vp.swa_layers[0]
+        g_full = capture(lambda: vp.attend_full_layer(lf))
+        g_swa = capture(lambda: vp.attend_swa_layer(ls))
+        k_steps = max(50, min(args.steps, 500))
+        f_mean, f_med, _ = event_time_graph(g_full, flush, k_steps)
+        s_mean, s_med, _ = event_time_graph(g_swa, flush, k_steps)
+        achieved = sz.bytes_full / (f_mean * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "attend_kernel<128,false> + combine (one full layer, 8K resident)",
+                    "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "algorithmic_bytes": sz.bytes_full, "peak_kind": peak_kind}
+        extras["full_layer_us"] = round(f_mean * 1000, 3)
+        extras["swa_layer_us"] = round(s_mean * 1000, 3)
+        extras["swa_layer_gbs"] = round(sz.bytes_swa / (s_mean * 1e-3) / 1e9, 1)
+        del g_full, g_swa
+        # the all-resident 256K full layer (4096 chunks = 512 MiB of KV): the clean bandwidth point
+        wl1 = synth.Workload("all-resident", synth.LAGUNA, [262144], [16], n_full=1, n_swa=0, resident_chunks=0)
+        ar = passes.VerifyPass(wl1, device=local, seed=rank + 1, all_resident=True)
+        g_ar = capture(lambda: ar.attend_full_layer(ar.full_layers[0]))
+        a_mean, a_med, _ = event_time_graph(g_ar, flush, max(20, min(args.steps, 200)))
+        a_bytes = ar.sizes().bytes_full
+        extras["all_resident_256k_layer"] = {"us": round(a_mean * 1000, 2), "bytes": a_bytes,
+                                             "gbs": round(a_bytes / (a_mean * 1e-3) / 1e9, 1),
+                                             "frac": round(a_bytes / (a_mean * 1e-3) / 1e9 / peak, 4)}
+        del g_ar
+        ar.close()
+
+    # end to end: inputs host->device from pinned memory, accepted tokens back, inside the timing
+    q_host = vp.q_all.cpu().pin_memory()
+    logits_host = vp.logits.cpu().pin_memory()
+    drafts_host = vp.drafts.cpu().pin_memory()
+    score_host = [vp.score_table[t].cpu().pin_memory() for t in range(vp.score_table.shape[0])]
+    out_host = torch.empty(vp.q + 2, dtype=torch.int32).pin_memory()
+    h2d = q_host.numel() * 2 + logits_host.numel() * 4 + drafts_host.numel() * 4 + score_host[0].numel() * 4
+    d2h = out_host.numel() * 4
+    e_steps = max(20, min(args.steps, 500))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+    res_dev = torch.empty(vp.q + 2, dtype=torch.int32, device="cuda")
+    for i in range(e_steps):
+        flush.zero_()
+        starts[i].record()
+        vp.q_all.copy_(q_host, non_blocking=True)
+        vp.scores.copy_(score_host[vp.step % len(score_host)], non_blocking=True)
+        vp.step += 1
+        vp.logits.copy_(logits_host, non_blocking=True)
+        vp.drafts.copy_(drafts_host, non_blocking=True)
+        vp.replay()
+        res_dev[0:1].copy_(vp.accepted)
+        res_dev[1:2].copy_(vp.bonus)
+        res_dev[2:].copy_(vp.committed)
+        out_host.copy_(res_dev, non_blocking=True)
+        ends[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+    e2e_ms = dist_max(e2e_ms, torch.device("cuda", local))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_baseline_obj(run_oracle_child(12.0))
+        except Exception as e:  # reported, not fatal
+            cpu = {"error": str(e)[:200]}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": wl.name, "seq_len": wl.seq_lens[0], "draft": wl.depths[0],
+                           "layers": sz.n_layers, "full_layers": sz.n_full, "window_layers": sz.n_swa,
+                           "resident_chunks": wl.resident_chunks, "pagein_per_step": wl.pagein_per_step,
+                           "heads": "16q/4kv x 128", "l2": "flushed between steps (256 MiB write)",
+                           "parallelism": f"replicas x{world}", "timing": "CUDA events around each graph replay"},
+                "kv_gbs": round(kv_gbs, 1), "kv_frac_of_hbm": round(kv_gbs / peak, 4),
+                "median_ms_per_step": round(med_ms, 5), "wall_s": round(wall, 3),
+                "pass_bytes": sz.bytes_pass, "accepted_last_step": accepted,
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
+                "e2e": {"value": round(aggregate_us_per_layer(e2e_ms, sz.n_layers, world), 4), "unit": UNIT,
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": launches}
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    vp.close()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_sample or "--oracle-sample" in (argv or sys.argv):
+        print(json.dumps(oracle_sample_seconds(args.oracle_sample)))
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

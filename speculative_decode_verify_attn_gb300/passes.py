@@ -1,0 +1,215 @@
+"""A whole verify pass over a synthetic model, captured once as a CUDA graph and replayed.
+
+The pass is the data-parallel hot path of one speculative-decoding step at long context
+('Laguna XS 2.1 33B on a RTX 3090' (lucebox): 40 layers in a 3-in-4 window pattern, 'Three
+optimizations' items 1 and 3; CUDA-graph replay of the decode loop):
+
+  vfy_select_resident                       residency for this step (one chunk table for all
+                                            full layers; each full layer has its own pool)
+  vfy_page_in x n_full      (side stream)   the step's newly resident chunks, host -> pools
+  for layer l in 0..n_layers-1:             window layers where l % 4 != 3, full where l % 4 == 3
+      vfy_attend_swa / vfy_attend_full      (a full layer waits for its own page-in)
+  vfy_accept                                argmax + greedy acceptance over the block's logits
+
+Every per-step value (scores, lengths, lists, offsets, drafts) sits in device memory at a fixed
+address, so one graph serves every step. Inputs are synthetic (synth.py) with the shapes of the
+pages' workloads; model weights do not enter: the block's Q rows and KV are random bf16.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import synth, vfy
+
+CHUNK = 64
+
+
+def is_full_layer(layer: int) -> bool:
+    """3-in-4 pattern: layers 3, 7, 11, ... are full attention, the others window layers."""
+    return layer % 4 == 3
+
+
+@dataclass
+class PassSizes:
+    n_layers: int
+    n_full: int
+    n_swa: int
+    bytes_full: int       # algorithmic bytes of one full layer (KV read + Q read + O write)
+    bytes_swa: int
+    bytes_accept: int
+    bytes_pass: int
+
+
+class VerifyPass:
+    """Single-sequence 256K pass (one replica per GPU)."""
+
+    def __init__(self, workload: synth.Workload, device: int = 0, seed: int = 0, all_resident: bool = False,
+                 match_prob: float = 0.56):
+        assert workload.num_seqs == 1
+        self.w = workload
+        self.dev = torch.device("cuda", device)
+        s = workload.shape
+        self.shape = s
+        self.L = workload.seq_lens[0]
+        self.q = workload.queries[0]
+        self.n_chunks = (self.L + CHUNK - 1) // CHUNK
+        self.all_resident = all_resident
+        self.k = self.n_chunks if all_resident else workload.resident_chunks
+        self.n_layers = workload.n_full + workload.n_swa
+        self.vocab = workload.vocab
+        rng = np.random.default_rng(seed)
+        gen = torch.Generator(device=self.dev)
+        gen.manual_seed(seed)
+        dev = self.dev
+        hkv, d, hq = s.num_kv_heads, s.head_dim, s.num_q_heads
+        torch.cuda.set_device(dev)
+
+        self.ctx = vfy.vfy_create(hq, hkv, d, window=synth.WINDOW, ring_len=synth.RING, max_seqs=1,
+                                  max_queries_per_seq=self.q, max_splits=64, device=device)
+        # --- per-step residency inputs ---
+        self.rot = synth.rotating_residency(rng, self.n_chunks, self.k, workload.pagein_per_step or 16,
+                                            self.L, self.q) if not all_resident else None
+        self.cu_chunks = torch.tensor([0, self.n_chunks], dtype=torch.int32, device=dev)
+        self.scores = torch.zeros(self.n_chunks, dtype=torch.float32, device=dev)
+        self.slot_of_chunk = torch.full((self.n_chunks,), -1, dtype=torch.int32, device=dev)
+        self.res_ids = torch.zeros(self.k, dtype=torch.int32, device=dev)
+        self.res_slots = torch.zeros(self.k, dtype=torch.int32, device=dev)
+        self.cu_res = torch.tensor([0, self.k], dtype=torch.int32, device=dev)
+        self.pagein_list = torch.zeros((self.k, 2), dtype=torch.int32, device=dev)
+        self.pagein_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        if all_resident:
+            self.res_ids.copy_(torch.arange(self.k, dtype=torch.int32, device=dev))
+            self.res_slots.copy_(torch.arange(self.k, dtype=torch.int32, device=dev))
+        self.score_table = (torch.from_numpy(np.stack([self.rot.scores(t) for t in range(len(self.rot.groups))]))
+                            .to(dev)) if self.rot is not None else None
+        # --- KV: per full layer a pool (+ a pinned host store when paging), per window layer a ring
+        self.full_layers = [l for l in range(self.n_layers) if is_full_layer(l)]
+        self.swa_layers = [l for l in range(self.n_layers) if not is_full_layer(l)]
+        pool_shape = (self.k, hkv, CHUNK, d)
+        self.pool_k, self.pool_v, self.host_k, self.host_v = {}, {}, {}, {}
+        for l in self.full_layers:
+            if all_resident:
+                self.pool_k[l] = torch.randn(pool_shape, generator=gen, device=dev, dtype=torch.bfloat16)
+                self.pool_v[l] = torch.randn(pool_shape, generator=gen, device=dev, dtype=torch.bfloat16)
+            else:
+                self.pool_k[l] = torch.zeros(pool_shape, device=dev, dtype=torch.bfloat16)
+                self.pool_v[l] = torch.zeros(pool_shape, device=dev, dtype=torch.bfloat16)
+                store = (self.n_chunks, hkv, CHUNK, d)
+                self.host_k[l] = torch.empty(store, dtype=torch.bfloat16, pin_memory=True)
+                self.host_v[l] = torch.empty(store, dtype=torch.bfloat16, pin_memory=True)
+                self.host_k[l].copy_(torch.randn(store, generator=gen, device=dev, dtype=torch.bfloat16))
+                self.host_v[l].copy_(torch.randn(store, generator=gen, device=dev, dtype=torch.bfloat16))
+        self.ring_k, self.ring_v = {}, {}
+        ring_shape = (1, hkv, synth.RING, d)
+        for l in self.swa_layers:
+            self.ring_k[l] = torch.randn(ring_shape, generator=gen, device=dev, dtype=torch.bfloat16)
+            self.ring_v[l] = torch.randn(ring_shape, generator=gen, device=dev, dtype=torch.bfloat16)
+        phi = synth.wrapping_ring_offset(rng, self.L, synth.WINDOW + self.q - 1, synth.RING)
+        self.ring_offset = torch.tensor([phi], dtype=torch.int32, device=dev)
+        # --- block: queries per layer, outputs, lengths ---
+        self.cu_q = torch.tensor([0, self.q], dtype=torch.int32, device=dev)
+        self.seq_len = torch.tensor([self.L], dtype=torch.int32, device=dev)
+        # one buffer for all layers' block queries (one host->device copy per step end to end)
+        self.q_all = torch.randn((self.n_layers, self.q, hq, d), generator=gen, device=dev, dtype=torch.bfloat16)
+        self.qs = [self.q_all[l] for l in range(self.n_layers)]
+        self.out_all = torch.empty((self.n_layers, self.q, hq, d), device=dev, dtype=torch.bfloat16)
+        self.outs = [self.out_all[l] for l in range(self.n_layers)]
+        self.lse_all = torch.empty((self.n_layers, self.q, hq), device=dev, dtype=torch.float32)
+        self.lses = [self.lse_all[l] for l in range(self.n_layers)]
+        # --- acceptance ---
+        targets = rng.integers(0, self.vocab, self.q)
+        self.targets = targets
+        self.logits = torch.from_numpy(synth.planted_logits(rng, targets, self.vocab)).to(dev)
+        self.drafts = torch.from_numpy(synth.drafts_matching(rng, targets, match_prob, self.vocab)).to(dev)
+        self.cu_rows = torch.tensor([0, self.q], dtype=torch.int32, device=dev)
+        self.accepted = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.bonus = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.committed = torch.zeros(self.q, dtype=torch.int32, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.graph = None
+        self.step = 0
+
+    # ------------------------------------------------------------------------------------------
+    def sizes(self) -> PassSizes:
+        s = self.shape
+        per_tok = s.num_kv_heads * s.head_dim * 2 * 2                    # K + V bf16
+        qo = 2 * self.q * s.num_q_heads * s.head_dim * 2                 # Q read + O write
+        bytes_full = self.k * CHUNK * per_tok + qo
+        span = min(self.L, synth.WINDOW + self.q - 1)
+        bytes_swa = span * per_tok + qo
+        bytes_accept = self.q * self.vocab * 4
+        n_full, n_swa = len(self.full_layers), len(self.swa_layers)
+        return PassSizes(self.n_layers, n_full, n_swa, bytes_full, bytes_swa, bytes_accept,
+                         n_full * bytes_full + n_swa * bytes_swa + bytes_accept)
+
+    def launches_per_step(self) -> int:
+        paging = 0 if self.all_resident else 1 + len(self.full_layers)
+        return paging + 2 * self.n_layers + 1
+
+    def set_step_scores(self, t: int):
+        """Load step t's residency scores into the fixed score buffer (outside the graph)."""
+        if self.score_table is not None:
+            self.scores.copy_(self.score_table[t % self.score_table.shape[0]], non_blocking=True)
+
+    def attend_full_layer(self, l: int, stream=None):
+        vfy.vfy_attend_full(self.ctx, self.qs[l], self.cu_q, self.pool_k[l], self.pool_v[l], self.k,
+                            self.res_ids, self.res_slots, self.cu_res, self.k, self.seq_len, self.outs[l],
+                            self.lses[l], 1, stream)
+
+    def attend_swa_layer(self, l: int, stream=None):
+        vfy.vfy_attend_swa(self.ctx, self.qs[l], self.cu_q, self.ring_k[l], self.ring_v[l], self.ring_offset,
+                           self.seq_len, self.outs[l], self.lses[l], 1, stream)
+
+    def enqueue(self):
+        """Enqueue one pass on the current stream (used for capture and for eager runs)."""
+        main = torch.cuda.current_stream(self.dev)
+        events = {}
+        if not self.all_resident:
+            vfy.vfy_select_resident(self.ctx, self.scores, self.cu_chunks, 1, self.n_chunks, self.k,
+                                    self.slot_of_chunk, self.res_ids, self.res_slots, self.cu_res,
+                                    self.pagein_list, self.pagein_count, main)
+            self.side.wait_stream(main)
+            with torch.cuda.stream(self.side):
+                for l in self.full_layers:
+                    vfy.vfy_page_in(self.ctx, self.host_k[l], self.host_v[l], self.n_chunks, self.pool_k[l],
+                                    self.pool_v[l], self.k, self.pagein_list, self.pagein_count, 1, self.k,
+                                    self.side)
+                    ev = torch.cuda.Event()
+                    ev.record(self.side)
+                    events[l] = ev
+        for l in range(self.n_layers):
+            if is_full_layer(l):
+                if l in events:
+                    main.wait_event(events[l])
+                self.attend_full_layer(l, main)
+            else:
+                self.attend_swa_layer(l, main)
+        vfy.vfy_accept(self.ctx, self.logits, self.vocab, self.drafts, self.cu_rows, self.q, self.accepted,
+                       self.bonus, self.committed, 1, main)
+        if not self.all_resident:
+            main.wait_stream(self.side)
+
+    def capture(self):
+        # one eager pass first (also sets kernel attributes outside capture)
+        self.set_step_scores(0)
+        self.enqueue()
+        torch.cuda.synchronize(self.dev)
+        self.graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.graph, stream=s):
+                self.enqueue()
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        torch.cuda.synchronize(self.dev)
+        self.step = 1
+
+    def replay(self):
+        self.graph.replay()
+
+    def close(self):
+        self.graph = None
+        self.ctx.close()
