@@ -48,6 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the all-resident and per-kernel points")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host copies) measurement")
     ap.add_argument("--oracle-sample", type=float, default=0.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -297,6 +298,41 @@ def capture(fn):
     return g
 
 
+def measure_e2e(vp, flush, args, local, sz, world):
+    import torch
+    q_host = vp.q_all.cpu().pin_memory()
+    logits_host = vp.logits.cpu().pin_memory()
+    drafts_host = vp.drafts.cpu().pin_memory()
+    score_host = [vp.score_table[t].cpu().pin_memory() for t in range(vp.score_table.shape[0])]
+    out_host = torch.empty(vp.q + 2, dtype=torch.int32).pin_memory()
+    h2d = q_host.numel() * 2 + logits_host.numel() * 4 + drafts_host.numel() * 4 + score_host[0].numel() * 4
+    d2h = out_host.numel() * 4
+    e_steps = max(20, min(args.steps, 500))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+    res_dev = torch.empty(vp.q + 2, dtype=torch.int32, device="cuda")
+    for i in range(e_steps):
+        flush.zero_()
+        starts[i].record()
+        vp.q_all.copy_(q_host, non_blocking=True)
+        vp.scores.copy_(score_host[vp.step % len(score_host)], non_blocking=True)
+        vp.step += 1
+        vp.logits.copy_(logits_host, non_blocking=True)
+        vp.drafts.copy_(drafts_host, non_blocking=True)
+        vp.replay()
+        res_dev[0:1].copy_(vp.accepted)
+        res_dev[1:2].copy_(vp.bonus)
+        res_dev[2:].copy_(vp.committed)
+        out_host.copy_(res_dev, non_blocking=True)
+        ends[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+    e2e_ms = dist_max(e2e_ms, torch.device("cuda", local))
+
+    return {"value": round(aggregate_us_per_layer(e2e_ms, sz.n_layers, world), 4), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
 def run_ours(args):
     import torch
 
@@ -364,7 +400,7 @@ def run_ours(args):
         extras["swa_layer_gbs"] = round(sz.bytes_swa / (s_mean * 1e-3) / 1e9, 1)
         del g_full, g_swa
         # the all-resident 256K full layer (4096 chunks = 512 MiB of KV): the clean bandwidth point
-        wl1 = synth.Workload("all-resident", synth.LAGUNA, [262144], [16], n_full=1, n_swa=0, resident_chunks=0)
+        wl1 = synth.Workload("all-resident", synth.LAGUNA, [262144], [16], n_full=1, n_swa=3, resident_chunks=0)
         ar = passes.VerifyPass(wl1, device=local, seed=rank + 1, all_resident=True)
         g_ar = capture(lambda: ar.attend_full_layer(ar.full_layers[0]))
         a_mean, a_med, _ = event_time_graph(g_ar, flush, max(20, min(args.steps, 200)))
@@ -376,34 +412,9 @@ def run_ours(args):
         ar.close()
 
     # end to end: inputs host->device from pinned memory, accepted tokens back, inside the timing
-    q_host = vp.q_all.cpu().pin_memory()
-    logits_host = vp.logits.cpu().pin_memory()
-    drafts_host = vp.drafts.cpu().pin_memory()
-    score_host = [vp.score_table[t].cpu().pin_memory() for t in range(vp.score_table.shape[0])]
-    out_host = torch.empty(vp.q + 2, dtype=torch.int32).pin_memory()
-    h2d = q_host.numel() * 2 + logits_host.numel() * 4 + drafts_host.numel() * 4 + score_host[0].numel() * 4
-    d2h = out_host.numel() * 4
-    e_steps = max(20, min(args.steps, 500))
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
-    res_dev = torch.empty(vp.q + 2, dtype=torch.int32, device="cuda")
-    for i in range(e_steps):
-        flush.zero_()
-        starts[i].record()
-        vp.q_all.copy_(q_host, non_blocking=True)
-        vp.scores.copy_(score_host[vp.step % len(score_host)], non_blocking=True)
-        vp.step += 1
-        vp.logits.copy_(logits_host, non_blocking=True)
-        vp.drafts.copy_(drafts_host, non_blocking=True)
-        vp.replay()
-        res_dev[0:1].copy_(vp.accepted)
-        res_dev[1:2].copy_(vp.bonus)
-        res_dev[2:].copy_(vp.committed)
-        out_host.copy_(res_dev, non_blocking=True)
-        ends[i].record()
-    torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
-    e2e_ms = dist_max(e2e_ms, torch.device("cuda", local))
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(vp, flush, args, local, sz, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -425,8 +436,7 @@ def run_ours(args):
                 "median_ms_per_step": round(med_ms, 5), "wall_s": round(wall, 3),
                 "pass_bytes": sz.bytes_pass, "accepted_last_step": accepted,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
-                "e2e": {"value": round(aggregate_us_per_layer(e2e_ms, sz.n_layers, world), 4), "unit": UNIT,
-                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "e2e": e2e,
                 "gpu_launches": launches}
         line.update(extras)
         print(json.dumps(line), flush=True)

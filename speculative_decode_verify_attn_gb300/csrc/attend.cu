@@ -52,7 +52,8 @@ struct Bars {
   uint64_t kv_empty[8];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_full;
+  uint64_t o_full;     // one phase per P.V MMA (the softmax waits on it before rescaling O)
+  uint64_t o_done;     // one phase, after the last P.V MMA (the epilogue waits on it)
   uint64_t q_ready;
   uint64_t drain;
   uint32_t tmem_base;
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[i], 128);
     }
     mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->q_ready, 128);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bars->kv_empty[st]);
           mma_commit(&bars->o_full);
+          if (jp == w.nt - 1) mma_commit(&bars->o_done);
         }
         __syncwarp();
       }
@@ -369,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, need_o)) {
         // O holds the sum over tiles < j: wait for PV_{j-1}, then scale the rows that need it.
+        // S_j has completed, so PV_{j-2} has too; o_full is in phase j-1 or j, and the parity
+        // wait for phase j-1 is exact.
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full, (j - 1) & 1, abort, p.err));
         if (!ok) break;
         tc_fence_after();
@@ -398,8 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->p_full[j & 1]);
     }
     // ---- epilogue: the split's partial (m, l, unnormalised O) ----
+    // A parity wait on o_full cannot tell phase nt-1 from nt-3 when P.V_{nt-2} is still running,
+    // so the last P.V has a barrier of its own.
     if (ok && w.nt > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full, (w.nt - 1) & 1, abort, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort, p.err));
       tc_fence_after();
     }
     if (ok) {

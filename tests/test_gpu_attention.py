@@ -287,3 +287,21 @@ def test_swa_ragged_batch(H, vfy):
     ref, rlse = O.attend_ring(qb, cu_q, rk, rv, phis, lens, 512)
     assert_attn_close(got, ref, "swa ragged")
     assert_lse_close(lse, rlse, "swa ragged")
+
+
+@pytest.mark.parametrize("tiles_per_split", [1, 2, 3])
+def test_repeated_short_splits_are_stable(H, vfy, tiles_per_split):
+    """Splits of one to three tiles, repeated: the epilogue must wait for the last P.V MMA even
+    when the previous one is still running."""
+    rng = np.random.default_rng(20 + tiles_per_split)
+    s = synth.LAGUNA
+    L, q, R = 9000, 17, 2048
+    rk, rv = ring_case(rng, s, 1)
+    qb = synth.normal_bf16(rng, (q, s.num_q_heads, s.head_dim))
+    phi = 1500                                     # 10 slot-aligned tiles
+    ctx = make_ctx(vfy, s)
+    vfy.vfy_set_splits(ctx, 0, 10 // tiles_per_split)
+    ref, _ = O.attend_ring_seq(qb, rk[0], rv[0], phi, L, 512)
+    for rep in range(25):
+        got, _ = H.attend_swa(ctx, qb, [0, q], rk, rv, [phi], [L])
+        assert_attn_close(got, ref, f"rep {rep}")
