@@ -395,6 +395,20 @@ def run_ours(args):
                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": None,
                     "algorithmic_bytes": sz.bytes_full, "peak_kind": peak_kind}
+        g_layers = capture(vp.enqueue_layers)
+        l_mean, _, _ = event_time_graph(g_layers, flush, k_steps)
+        g_acc = capture(vp.enqueue_accept)
+        c_mean, _, _ = event_time_graph(g_acc, flush, k_steps)
+        g_pg = capture(vp.enqueue_paging)
+        p_mean, _, _ = event_time_graph(g_pg, flush, min(k_steps, 100), pre=next_scores)
+        pg_bytes = len(vp.full_layers) * wl.pagein_per_step * vp.shape.num_kv_heads * 64 * vp.shape.head_dim * 4
+        extras["layers_only_us_per_layer"] = round(l_mean * 1000 / sz.n_layers, 3)
+        extras["layers_only_kv_gbs"] = round((sz.bytes_pass - sz.bytes_accept) / (l_mean * 1e-3) / 1e9, 1)
+        extras["accept_us"] = round(c_mean * 1000, 3)
+        extras["accept_gbs"] = round(sz.bytes_accept / (c_mean * 1e-3) / 1e9, 1)
+        extras["select_plus_pagein_us"] = round(p_mean * 1000, 3)
+        extras["pagein_host_gbs"] = round(pg_bytes / (p_mean * 1e-3) / 1e9, 1)
+        del g_layers, g_acc, g_pg
         extras["full_layer_us"] = round(f_mean * 1000, 3)
         extras["swa_layer_us"] = round(s_mean * 1000, 3)
         extras["swa_layer_gbs"] = round(sz.bytes_swa / (s_mean * 1e-3) / 1e9, 1)

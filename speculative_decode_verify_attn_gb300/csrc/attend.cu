@@ -19,6 +19,8 @@
 // real rows spread over the four lane quarters and all four softmax warps share the work.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "vfy_internal.cuh"
 
@@ -155,6 +157,27 @@ __device__ __forceinline__ bool key_in_union(const AttnParams& p, const Work& w,
     if (off >= p.ring_len) off -= p.ring_len;
     *pos_out = w.lo + off;
     return off < w.span;
+  }
+}
+
+// The keys of a tile that one row attends form an interval [klo, khi] of tile indices:
+//  full: positions base + k <= p_i (and the tile's chunk is valid);
+//  ring: offsets (from s_lo) in [max(0, p_i - W + 1 - lo), p_i - lo]. In the one tile that holds
+//  both ring ends (base + 63 >= R) the indices below R - base map to offsets near R, which lie
+//  outside every window (the ring holds at least the span plus one tile), so shifting by R
+//  keeps the valid keys an interval.
+template <bool RING>
+__device__ __forceinline__ void key_interval(const AttnParams& p, const Work& w, const Tile& t, int p_i, int* klo,
+                                             int* khi) {
+  if (!RING) {
+    *klo = 0;
+    *khi = t.valid ? min(kChunk - 1, p_i - t.base) : -1;
+  } else {
+    const int shift = t.base + kChunk - 1 < p.ring_len ? t.base : t.base - p.ring_len;
+    const int a = max(0, p_i - p.window + 1 - w.lo);
+    const int b = p_i - w.lo;
+    *klo = a - shift;
+    *khi = b - shift;
   }
 }
 
@@ -347,21 +370,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s_lo[32], s_hi[32];
-      tmem_ld32(lane_base + kColS + (j & 1) * 64, s_lo);
-      tmem_ld32(lane_base + kColS + (j & 1) * 64 + 32, s_hi);
+      uint32_t sr[64];
+      tmem_ld64(lane_base + kColS + (j & 1) * 64, sr);
       const Tile t = tile_at<RING>(p, w, j);
-      float x[64];
-      float m_tile = -INFINITY;
+      int klo = 0, khi = kChunk - 1;
+      if (rv) key_interval<RING>(p, w, t, p_i, &klo, &khi);
+      // Rows past the block (padding lanes) see Q = 0; their P and O rows are never read.
+      float sv[64];
+      if (__all_sync(0xffffffffu, klo <= 0 && khi >= kChunk - 1)) {
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        int pos;
-        bool v = key_in_union<RING>(p, w, t, k, &pos) && rv && pos <= p_i;
-        if (RING) v = v && pos > p_i - p.window;
-        const uint32_t bits = k < 32 ? s_lo[k] : s_hi[k - 32];
-        x[k] = v ? __uint_as_float(bits) * p.scale_log2 : -INFINITY;
-        m_tile = fmaxf(m_tile, x[k]);
+        for (int k = 0; k < 64; ++k) sv[k] = __uint_as_float(sr[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) sv[k] = (k >= klo && k <= khi) ? __uint_as_float(sr[k]) : -INFINITY;
       }
+      // tile maximum of the raw scores (a tree, for instruction-level parallelism)
+      float mx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(fmaxf(sv[u], sv[u + 8]), fmaxf(sv[u + 16], sv[u + 24]));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], fmaxf(fmaxf(sv[u + 32], sv[u + 40]), fmaxf(sv[u + 48], sv[u + 56])));
+      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
       bool need_o = false;
       float alpha = 1.f;
       if (m_tile > m_ref + kRescaleLog2) {
@@ -387,17 +417,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(lane_base + kColO + c * 32, o);
         }
       }
+      // p = 2^(s * scale * log2e - m_ref); masked keys carry s = -inf and give exactly 0. A row that
+      // has seen no key yet (m_ref = -inf) has only masked keys here, and uses 0 as reference.
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
       uint32_t pk[32];
-      float psum = 0.f;
+      float ps[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float p0 = x[2 * e] == -INFINITY ? 0.f : ex2_approx(x[2 * e] - m_ref);
-        const float p1 = x[2 * e + 1] == -INFINITY ? 0.f : ex2_approx(x[2 * e + 1] - m_ref);
+        const float p0 = ex2_approx(fmaf(sv[2 * e], p.scale_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, neg_m));
+        ps[e & 7] += p0 + p1;
         const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        psum += __low2float(h2) + __high2float(h2);
         pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      l_sum += psum;
+      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      if (rv) l_sum += psum;
       tmem_st32(lane_base + kColP + (j & 1) * 32, pk);
       tc_fence_before();
       mbar_arrive(&bars->p_full[j & 1]);
@@ -464,6 +500,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const size_t p0 = (static_cast<size_t>(b) * p.hkv + h) * p.num_splits;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
 
+  // Pass 1: the largest m over splits that hold data (each lane reads splits lane, lane + 32, ...).
   float mmax = -INFINITY;
   for (int s = lane; s < p.num_splits; s += 32) {
     const float2 v = ml[(p0 + s) * kMaxRows + r];
@@ -472,7 +509,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
 
+  // Pass 2: weights in the lanes, then batches of 8 independent 16-byte loads per lane.
   constexpr int kPer = HD / 32;
+  using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
@@ -480,30 +519,42 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   if (mmax != -INFINITY) {
     for (int s0 = 0; s0 < p.num_splits; s0 += 32) {
       const int s = s0 + lane;
-      float wgt = 0.f, lw = 0.f;
+      float wgt = 0.f;
       if (s < p.num_splits) {
         const float2 v = ml[(p0 + s) * kMaxRows + r];
         if (v.y > 0.f) {
           wgt = ex2_approx(v.x - mmax);
-          lw = wgt * v.y;
+          lsum += wgt * v.y;
         }
       }
-      lsum += lw;
       const int cnt = min(32, p.num_splits - s0);
-      for (int k = 0; k < cnt; ++k) {
-        const float wk = __shfl_sync(0xffffffffu, wgt, k);
-        if (wk == 0.f) continue;   // never read a split that holds no row data
-        const float* src = p.part_o + ((p0 + s0 + k) * kMaxRows + r) * HD + lane * kPer;
-        if constexpr (kPer == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src);
-          acc[0] += wk * v.x;
-          acc[1] += wk * v.y;
-          acc[2] += wk * v.z;
-          acc[3] += wk * v.w;
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(src);
-          acc[0] += wk * v.x;
-          acc[1] += wk * v.y;
+      for (int k0 = 0; k0 < cnt; k0 += 8) {
+        Vec v[8];
+        float wk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          wk[u] = __shfl_sync(0xffffffffu, wgt, (k0 + u) & 31);
+          const bool use = (k0 + u) < cnt && wk[u] != 0.f;   // never read a split without row data
+          const Vec* src = reinterpret_cast<const Vec*>(p.part_o + ((p0 + s0 + k0 + u) * kMaxRows + r) * HD) + lane;
+          if (use) {
+            v[u] = __ldcg(src);
+          } else {
+            wk[u] = 0.f;
+            if constexpr (kPer == 4) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            else v[u] = make_float2(0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if constexpr (kPer == 4) {
+            acc[0] = fmaf(wk[u], v[u].x, acc[0]);
+            acc[1] = fmaf(wk[u], v[u].y, acc[1]);
+            acc[2] = fmaf(wk[u], v[u].z, acc[2]);
+            acc[3] = fmaf(wk[u], v[u].w, acc[3]);
+          } else {
+            acc[0] = fmaf(wk[u], v[u].x, acc[0]);
+            acc[1] = fmaf(wk[u], v[u].y, acc[1]);
+          }
         }
       }
     }

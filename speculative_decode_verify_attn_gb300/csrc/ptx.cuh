@@ -197,6 +197,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+#define VFY_R8B(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                   "=r"(r[i + 6]), "=r"(r[i + 7])
+// Load 64 consecutive 32-bit columns of this warp's 32 TMEM lanes and wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : VFY_R8B(0), VFY_R8B(8), VFY_R8B(16), VFY_R8B(24), VFY_R8B(32), VFY_R8B(40), VFY_R8B(48), VFY_R8B(56)
+      : "r"(taddr)
+      : "memory");
+}
+#undef VFY_R8B
+
 // Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes and wait for completion.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(

@@ -163,6 +163,29 @@ class VerifyPass:
         vfy.vfy_attend_swa(self.ctx, self.qs[l], self.cu_q, self.ring_k[l], self.ring_v[l], self.ring_offset,
                            self.seq_len, self.outs[l], self.lses[l], 1, stream)
 
+    def enqueue_paging(self):
+        """Residency selection and the page-ins of every full layer, on the current stream only."""
+        main = torch.cuda.current_stream(self.dev)
+        vfy.vfy_select_resident(self.ctx, self.scores, self.cu_chunks, 1, self.n_chunks, self.k,
+                                self.slot_of_chunk, self.res_ids, self.res_slots, self.cu_res,
+                                self.pagein_list, self.pagein_count, main)
+        for l in self.full_layers:
+            vfy.vfy_page_in(self.ctx, self.host_k[l], self.host_v[l], self.n_chunks, self.pool_k[l],
+                            self.pool_v[l], self.k, self.pagein_list, self.pagein_count, 1, self.k, main)
+
+    def enqueue_layers(self):
+        """The attention layers alone, in pass order, on the current stream."""
+        main = torch.cuda.current_stream(self.dev)
+        for l in range(self.n_layers):
+            if is_full_layer(l):
+                self.attend_full_layer(l, main)
+            else:
+                self.attend_swa_layer(l, main)
+
+    def enqueue_accept(self):
+        vfy.vfy_accept(self.ctx, self.logits, self.vocab, self.drafts, self.cu_rows, self.q, self.accepted,
+                       self.bonus, self.committed, 1, torch.cuda.current_stream(self.dev))
+
     def enqueue(self):
         """Enqueue one pass on the current stream (used for capture and for eager runs)."""
         main = torch.cuda.current_stream(self.dev)
