@@ -123,7 +123,7 @@ vfy_status vfy_create(const vfy_config* cfg_in, int device, vfy_ctx** out) {
   VFY_REQUIRE(cfg.head_dim == 64 || cfg.head_dim == 128);
   VFY_REQUIRE(cfg.chunk_tokens == kChunk);
   VFY_REQUIRE(cfg.max_seqs >= 1 && cfg.max_queries_per_seq >= 1 && cfg.max_splits >= 1);
-  VFY_REQUIRE(cfg.max_splits <= 1024 && cfg.max_seqs <= 65535 && cfg.num_kv_heads <= 65535);
+  VFY_REQUIRE(cfg.max_splits <= 64 && cfg.max_seqs <= 65535 && cfg.num_kv_heads <= 65535);
   const int group = cfg.num_q_heads / cfg.num_kv_heads;
   VFY_REQUIRE(static_cast<long long>(cfg.max_queries_per_seq) * group <= kMaxRows);
   VFY_REQUIRE(cfg.window >= 1 && cfg.ring_len >= kChunk && cfg.ring_len % kChunk == 0);

@@ -12,9 +12,12 @@
 //    tiles are 64-slot aligned, so a tile never crosses the ring's end.
 //
 // One CTA handles one (sequence b, KV head h, split s): a contiguous run of tiles. Warp roles:
-//   warps 0-3  load Q, then one thread per TMEM lane / row: masked online softmax, epilogue
-//   warp 4     TMA producer (K and V tiles into a ring of smem stages)
-//   warp 5     TMEM owner and MMA issuer (one elected lane)
+//   warps 0-7  load Q, then the masked online softmax and the epilogue. Warps w and w + 4 share
+//              TMEM lane quarter w % 4 (one row per lane); warpgroup 0 takes the first 32 keys of
+//              each 64-key tile, warpgroup 1 the last 32. The two halves of a row exchange their
+//              maxima through shared memory under a per-quarter mbarrier.
+//   warp 8     TMA producer (K and V tiles into a ring of smem stages)
+//   warp 9     TMEM owner and MMA issuer (one elected lane)
 // Row r = i * G + g (query i, q-head g of the group) sits in TMEM lane (r % 4) * 32 + r / 4, so the
 // real rows spread over the four lane quarters and all four softmax warps share the work.
 #include <cuda_bf16.h>
@@ -27,7 +30,10 @@
 namespace vfy {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // O accumulator: d columns
 constexpr uint32_t kColS = 128;   // two S buffers of 64 columns
@@ -45,7 +51,7 @@ struct Cfg {
   static constexpr int kTileBytes = kChunk * HD * 2;
   static constexpr int kStages = HD == 128 ? 5 : 8;
   static constexpr int kBarOffset = kQBytes + 2 * kStages * kTileBytes;
-  static constexpr int kSmemBytes = kBarOffset + 1024 + 1024;
+  static constexpr int kSmemBytes = kBarOffset + 4096 + 1024;
 };
 
 struct Bars {
@@ -58,8 +64,14 @@ struct Bars {
   uint64_t o_done;     // one phase, after the last P.V MMA (the epilogue waits on it)
   uint64_t q_ready;
   uint64_t drain;
+  uint64_t xchg[4];     // per lane quarter: the two warpgroups' half-tile maxima (one phase per tile)
+  uint64_t xchg_l[4];   // per lane quarter: the two halves of l at the end
   uint32_t tmem_base;
   int abort;
+  int tile_base[8];     // per stage: what the mask needs of the tile in it (written by the producer
+  int tile_valid[8];    // before it arrives on k_full, read by the consumers after waiting on it)
+  float xmax[2][2][128];  // [tile parity][warpgroup][TMEM lane]
+  float xl[2][128];       // [warpgroup][TMEM lane]
 };
 
 // The per-CTA work item.
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- prologue (overlaps the previous kernel under programmatic dependent launch) ----------
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == kProducerWarp * 32) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->v_full[i], 1);
@@ -205,18 +217,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_full[i], kSoftmaxThreads);
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->q_ready, kSoftmaxThreads);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars->xchg[i], 64);
+      mbar_init(&bars->xchg_l[i], 64);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -234,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t idesc_pv = idesc_bf16_f32(128, HD, 0, 1);
   const size_t pidx = (static_cast<size_t>(w.b) * p.hkv + w.h) * p.num_splits + w.s;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------ TMA producer -----------------------------------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
@@ -248,6 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicOr(p.err, kErrDeviceInput);
           reported = true;
         }
+        bars->tile_base[st] = t.base;
+        bars->tile_valid[st] = t.valid ? 1 : 0;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
@@ -266,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer -------------------------------------------
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_ready, 0, abort, p.err));
     tc_fence_after();
@@ -303,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of the last chunk). P is 0 there, but 0 * NaN is NaN on the tensor core, so their V rows
         // are zeroed before the MMA reads them.
         {
-          const Tile t = tile_at<RING>(p, w, jp);
+          Tile t;
+          t.base = bars->tile_base[st];
+          t.valid = bars->tile_valid[st] != 0;
           uint8_t* vt = sV + st * C::kTileBytes;
           bool any = false;
           for (int k = lane; k < kChunk; k += 32) {
@@ -342,103 +362,128 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_drain(&bars->drain, 0);
   } else {
-    // ------------------------------ softmax / epilogue (warps 0-3) ------------------------
-    const int mrow = threadIdx.x;                      // TMEM lane and Q smem row
-    const int r = (mrow & 31) * 4 + (mrow >> 5);        // block row held by this lane
+    // ------------------------------ softmax / epilogue (warps 0-7) ------------------------
+    const int wg = warp >> 2;                          // warpgroup: which 32 keys of a tile
+    const int quarter = warp & 3;                      // TMEM lane quarter
+    const int mrow = quarter * 32 + lane;              // TMEM lane and Q smem row
+    const int r = lane * 4 + quarter;                  // block row held by this lane
     const bool rv = r < w.rows;
     const int qi = rv ? r / p.group : 0;
     const int g = rv ? r % p.group : 0;
     // Q row -> swizzled smem (the 128-byte swizzle TMA would apply: chunk c of row m at c ^ (m & 7)).
+    // Each warpgroup stages half of the row's 16-byte chunks.
     {
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (static_cast<size_t>(w.q0 + qi) * p.hq + static_cast<size_t>(w.h) * p.group + g) * HD);
+      constexpr int kHalf = HD / 16;
+      uint4 qv[kHalf];
 #pragma unroll
-      for (int c = 0; c < HD / 8; ++c) {
-        const uint4 v = rv ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        const int bx = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(sQ + bx * C::kQBoxBytes + mrow * 128 + ((cc ^ (mrow & 7)) << 4)) = v;
+      for (int c = 0; c < kHalf; ++c) qv[c] = rv ? __ldg(src + wg * kHalf + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c = 0; c < kHalf; ++c) {
+        const int cg = wg * kHalf + c;
+        const int bx = cg >> 3, cc = cg & 7;
+        *reinterpret_cast<uint4*>(sQ + bx * C::kQBoxBytes + mrow * 128 + ((cc ^ (mrow & 7)) << 4)) = qv[c];
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->q_ready);
     }
     const int p_i = w.L - w.nq + qi;                   // this row's query position
-    const uint32_t lane_base = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-    float m_ref = -INFINITY;
-    float l_sum = 0.f;
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int k0 = wg * 32;                            // this warpgroup's first key in a tile
+    float m_ref = -INFINITY;                           // shared by both halves of the row
+    float l_half = 0.f;                                // this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < w.nt; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld64(lane_base + kColS + (j & 1) * 64, sr);
-      const Tile t = tile_at<RING>(p, w, j);
+      uint32_t sr[32];
+      tmem_ld32(lane_base + kColS + (j & 1) * 64 + k0, sr);
+      // The tile's geometry comes from the producer through shared memory (k_full has completed,
+      // since S_j has: this wait only makes the producer's writes visible).
+      const int st = j % C::kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (j / C::kStages) & 1, abort, p.err));
+      if (!ok) break;
+      Tile t;
+      t.base = bars->tile_base[st];
+      t.valid = bars->tile_valid[st] != 0;
       int klo = 0, khi = kChunk - 1;
       if (rv) key_interval<RING>(p, w, t, p_i, &klo, &khi);
+      klo -= k0;
+      khi -= k0;
       // Rows past the block (padding lanes) see Q = 0; their P and O rows are never read.
-      float sv[64];
-      if (__all_sync(0xffffffffu, klo <= 0 && khi >= kChunk - 1)) {
+      float sv[32];
+      if (__all_sync(0xffffffffu, klo <= 0 && khi >= 31)) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) sv[k] = __uint_as_float(sr[k]);
+        for (int k = 0; k < 32; ++k) sv[k] = __uint_as_float(sr[k]);
       } else {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) sv[k] = (k >= klo && k <= khi) ? __uint_as_float(sr[k]) : -INFINITY;
+        for (int k = 0; k < 32; ++k) sv[k] = (k >= klo && k <= khi) ? __uint_as_float(sr[k]) : -INFINITY;
       }
-      // tile maximum of the raw scores (a tree, for instruction-level parallelism)
       float mx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx[u] = fmaxf(fmaxf(sv[u], sv[u + 8]), fmaxf(sv[u + 16], sv[u + 24]));
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], fmaxf(fmaxf(sv[u + 32], sv[u + 40]), fmaxf(sv[u + 48], sv[u + 56])));
-      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+      const float half_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // exchange the half maxima of the row with the other warpgroup
+      bars->xmax[j & 1][wg][mrow] = half_max;
+      mbar_arrive(&bars->xchg[quarter]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg[quarter], j & 1, abort, p.err));
+      if (!ok) break;
+      const float m_tile = fmaxf(half_max, bars->xmax[j & 1][wg ^ 1][mrow]) * p.scale_log2;
       bool need_o = false;
       float alpha = 1.f;
       if (m_tile > m_ref + kRescaleLog2) {
+        need_o = m_ref != -INFINITY;                  // O already holds weighted values
         alpha = ex2_approx(m_ref - m_tile);           // 0 when m_ref = -inf
-        need_o = l_sum > 0.f;
-        l_sum *= alpha;
+        l_half *= alpha;
         m_ref = m_tile;
       }
       if (__any_sync(0xffffffffu, need_o)) {
-        // O holds the sum over tiles < j: wait for PV_{j-1}, then scale the rows that need it.
-        // S_j has completed, so PV_{j-2} has too; o_full is in phase j-1 or j, and the parity
-        // wait for phase j-1 is exact.
+        // O holds the sum over tiles < j: wait for PV_{j-1}, then scale this warpgroup's half of
+        // the columns. S_j has completed, so PV_{j-2} has too; o_full is in phase j-1 or j, and the
+        // parity wait for phase j-1 is exact.
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full, (j - 1) & 1, abort, p.err));
         if (!ok) break;
         tc_fence_after();
         const float a = need_o ? alpha : 1.f;
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < HD / 64; ++c) {
+          const uint32_t col = kColO + wg * (HD / 2) + c * 32;
           uint32_t o[32];
-          tmem_ld32(lane_base + kColO + c * 32, o);
+          tmem_ld32(lane_base + col, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-          tmem_st32(lane_base + kColO + c * 32, o);
+          tmem_st32(lane_base + col, o);
         }
       }
       // p = 2^(s * scale * log2e - m_ref); masked keys carry s = -inf and give exactly 0. A row that
       // has seen no key yet (m_ref = -inf) has only masked keys here, and uses 0 as reference.
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t pk[32];
-      float ps[8];
+      uint32_t pk[16];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 16; ++e) {
         const float p0 = ex2_approx(fmaf(sv[2 * e], p.scale_log2, neg_m));
         const float p1 = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, neg_m));
-        ps[e & 7] += p0 + p1;
+        ps[e & 3] += p0 + p1;
         const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
         pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      if (rv) l_sum += psum;
-      tmem_st32(lane_base + kColP + (j & 1) * 32, pk);
+      if (rv) l_half += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      tmem_st16(lane_base + kColP + (j & 1) * 32 + wg * 16, pk);
       tc_fence_before();
       mbar_arrive(&bars->p_full[j & 1]);
     }
     // ---- epilogue: the split's partial (m, l, unnormalised O) ----
+    float l_sum = l_half;
+    if (ok) {
+      bars->xl[wg][mrow] = l_half;
+      mbar_arrive(&bars->xchg_l[quarter]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg_l[quarter], 0, abort, p.err));
+      if (ok) l_sum = l_half + bars->xl[wg ^ 1][mrow];
+    }
     // A parity wait on o_full cannot tell phase nt-1 from nt-3 when P.V_{nt-2} is still running,
     // so the last P.V has a barrier of its own.
     if (ok && w.nt > 0) {
@@ -446,12 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if (ok) {
-      float* dst = p.part_o + (pidx * kMaxRows + r) * HD;
+      float* dst = p.part_o + (pidx * kMaxRows + r) * HD + wg * (HD / 2);
       if (w.nt > 0) {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < HD / 64; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_base + kColO + c * 32, o);
+          tmem_ld32(lane_base + kColO + wg * (HD / 2) + c * 32, o);
           if (rv && l_sum > 0.f) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
@@ -461,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (rv) {
+      if (rv && wg == 0) {
         float2* ml = reinterpret_cast<float2*>(p.part_ml) + pidx * kMaxRows + r;
         *ml = make_float2(l_sum > 0.f ? m_ref : -INFINITY, l_sum);
       }
@@ -470,23 +515,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
 }
 
 // ------------------------------ split combine ---------------------------------------------------
-// One warp per output row (token t, q-head hq). Lanes first reduce the splits' maxima with
-// shuffles, then each lane accumulates HD/32 columns of sum_s 2^(m_s - M) o_s and the weights.
+// One 128-thread CTA per output row (token t, q-head hq). Warp w takes splits w, w + 4, ...; each
+// lane loads the (m, l) of one of them and 16 bytes of every one of them's O row, all loads in
+// one batch. The warp merges its splits against its own maximum (shuffles), then warp 0 merges the
+// four warps through shared memory:
 //   O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  LSE = ln2 * (M + log2 sum_s 2^(m_s - M) l_s)
+constexpr int kCombineMaxPerWarp = 16;   // splits per warp (64 splits per row at most)
+
 template <int HD>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+  constexpr int kPer = HD / 32;
+  using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
+  __shared__ float s_m[4];
+  __shared__ float s_l[4];
+  __shared__ float s_acc[4][HD];
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  const int t = static_cast<int>(row / p.hq);
-  const int hq = static_cast<int>(row % p.hq);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = static_cast<int>(blockIdx.x / p.hq);
+  const int hq = static_cast<int>(blockIdx.x % p.hq);
   if (t >= p.token_cap) return;
   const int total = p.cu_q[p.num_seqs];
   if (t >= total) return;
@@ -500,78 +553,79 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const size_t p0 = (static_cast<size_t>(b) * p.hkv + h) * p.num_splits;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
 
-  // Pass 1: the largest m over splits that hold data (each lane reads splits lane, lane + 32, ...).
-  float mmax = -INFINITY;
-  for (int s = lane; s < p.num_splits; s += 32) {
-    const float2 v = ml[(p0 + s) * kMaxRows + r];
-    if (v.y > 0.f) mmax = fmaxf(mmax, v.x);
-  }
+  // this warp's splits: s = warp + 4 u, u < nsub
+  const int nsub = min(kCombineMaxPerWarp, (p.num_splits - warp + 3) / 4);
+  float2 my_ml = make_float2(-INFINITY, 0.f);
+  if (lane < nsub) my_ml = __ldcg(ml + (p0 + warp + 4 * lane) * kMaxRows + r);
+  Vec v[kCombineMaxPerWarp];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
-
-  // Pass 2: weights in the lanes, then batches of 8 independent 16-byte loads per lane.
-  constexpr int kPer = HD / 32;
-  using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
+  for (int u = 0; u < kCombineMaxPerWarp; ++u) {
+    const float l_u = __shfl_sync(0xffffffffu, my_ml.y, u);
+    if (u < nsub && l_u > 0.f)   // never read a split that holds no row data
+      v[u] = __ldcg(reinterpret_cast<const Vec*>(p.part_o + ((p0 + warp + 4 * u) * kMaxRows + r) * HD) + lane);
+    else if constexpr (kPer == 4)
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    else
+      v[u] = make_float2(0.f, 0.f);
+  }
+  float m_w = my_ml.y > 0.f ? my_ml.x : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m_w = fmaxf(m_w, __shfl_xor_sync(0xffffffffu, m_w, o));
+  const float wgt = (my_ml.y > 0.f) ? ex2_approx(my_ml.x - m_w) : 0.f;
+  float l_w = wgt * my_ml.y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l_w += __shfl_xor_sync(0xffffffffu, l_w, o);
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  float lsum = 0.f;
-  if (mmax != -INFINITY) {
-    for (int s0 = 0; s0 < p.num_splits; s0 += 32) {
-      const int s = s0 + lane;
-      float wgt = 0.f;
-      if (s < p.num_splits) {
-        const float2 v = ml[(p0 + s) * kMaxRows + r];
-        if (v.y > 0.f) {
-          wgt = ex2_approx(v.x - mmax);
-          lsum += wgt * v.y;
-        }
-      }
-      const int cnt = min(32, p.num_splits - s0);
-      for (int k0 = 0; k0 < cnt; k0 += 8) {
-        Vec v[8];
-        float wk[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          wk[u] = __shfl_sync(0xffffffffu, wgt, (k0 + u) & 31);
-          const bool use = (k0 + u) < cnt && wk[u] != 0.f;   // never read a split without row data
-          const Vec* src = reinterpret_cast<const Vec*>(p.part_o + ((p0 + s0 + k0 + u) * kMaxRows + r) * HD) + lane;
-          if (use) {
-            v[u] = __ldcg(src);
-          } else {
-            wk[u] = 0.f;
-            if constexpr (kPer == 4) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            else v[u] = make_float2(0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if constexpr (kPer == 4) {
-            acc[0] = fmaf(wk[u], v[u].x, acc[0]);
-            acc[1] = fmaf(wk[u], v[u].y, acc[1]);
-            acc[2] = fmaf(wk[u], v[u].z, acc[2]);
-            acc[3] = fmaf(wk[u], v[u].w, acc[3]);
-          } else {
-            acc[0] = fmaf(wk[u], v[u].x, acc[0]);
-            acc[1] = fmaf(wk[u], v[u].y, acc[1]);
-          }
-        }
-      }
+  for (int u = 0; u < kCombineMaxPerWarp; ++u) {
+    const float wk = __shfl_sync(0xffffffffu, wgt, u);
+    if constexpr (kPer == 4) {
+      acc[0] = fmaf(wk, v[u].x, acc[0]);
+      acc[1] = fmaf(wk, v[u].y, acc[1]);
+      acc[2] = fmaf(wk, v[u].z, acc[2]);
+      acc[3] = fmaf(wk, v[u].w, acc[3]);
+    } else {
+      acc[0] = fmaf(wk, v[u].x, acc[0]);
+      acc[1] = fmaf(wk, v[u].y, acc[1]);
     }
+  }
+  if (lane == 0) {
+    s_m[warp] = m_w;
+    s_l[warp] = l_w;
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  for (int e = 0; e < kPer; ++e) s_acc[warp][lane * kPer + e] = acc[e];
+  __syncthreads();
+  if (warp != 0) return;
+  const float mmax = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+  float sc[4];
+  float lsum = 0.f;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    sc[x] = (s_l[x] > 0.f) ? ex2_approx(s_m[x] - mmax) : 0.f;
+    lsum += sc[x] * s_l[x];
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  float o[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    float a = 0.f;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) a = fmaf(sc[x], s_acc[x][lane * kPer + e], a);
+    o[e] = a * inv;
+  }
   uint16_t* dst = p.out + (static_cast<size_t>(t) * p.hq + hq) * HD + lane * kPer;
   if constexpr (kPer == 4) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-    const __nv_bfloat162 c = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-    uint2 v;
-    v.x = *reinterpret_cast<const uint32_t*>(&a);
-    v.y = *reinterpret_cast<const uint32_t*>(&c);
-    *reinterpret_cast<uint2*>(dst) = v;
+    const __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]);
+    const __nv_bfloat162 c = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 w2;
+    w2.x = *reinterpret_cast<const uint32_t*>(&a);
+    w2.y = *reinterpret_cast<const uint32_t*>(&c);
+    *reinterpret_cast<uint2*>(dst) = w2;
   } else {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    const __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]);
     *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&a);
   }
   if (p.lse != nullptr && lane == 0) {
@@ -605,7 +659,7 @@ cudaError_t launch_attend(bool ring, int head_dim, const AttnParams& p, const CU
 
 cudaError_t launch_combine(int head_dim, const CombineParams& p, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.token_cap) * p.hq;
-  dim3 grid(static_cast<unsigned>((rows + 3) / 4));
+  dim3 grid(static_cast<unsigned>(rows));
   if (head_dim == 128) return launch_pdl(combine_kernel<128>, grid, dim3(128), 0, stream, p);
   return launch_pdl(combine_kernel<64>, grid, dim3(128), 0, stream, p);
 }

@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <utility>
 
-#include "../../include/vfy.h"
+#include "vfy.h"
 
 namespace vfy {
 
