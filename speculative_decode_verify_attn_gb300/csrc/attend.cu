@@ -13,9 +13,10 @@
 //
 // One CTA handles one (sequence b, KV head h, split s): a contiguous run of tiles. Warp roles:
 //   warps 0-7  load Q, then the masked online softmax and the epilogue. Warps w and w + 4 share
-//              TMEM lane quarter w % 4 (one row per lane); warpgroup 0 takes the first 32 keys of
-//              each 64-key tile, warpgroup 1 the last 32. The two halves of a row exchange their
-//              maxima through shared memory under a per-quarter mbarrier.
+//              TMEM lane quarter w % 4 (one row per lane); warpgroup h takes keys [32h, 32h + 32)
+//              of every 64-key tile and keeps its own running maximum, row sum and O accumulator
+//              (O_h += P_h V_h, a K = 32 MMA), so the two halves never wait on each other; they
+//              are merged once, in the epilogue.
 //   warp 8     TMA producer (K and V tiles into a ring of smem stages)
 //   warp 9     TMEM owner and MMA issuer (one elected lane)
 // Row r = i * G + g (query i, q-head g of the group) sits in TMEM lane (r % 4) * 32 + r / 4, so the
@@ -35,9 +36,10 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;     // O accumulator: d columns
-constexpr uint32_t kColS = 128;   // two S buffers of 64 columns
-constexpr uint32_t kColP = 256;   // two P buffers of 32 columns (64 bf16 packed in pairs)
+constexpr uint32_t kColO = 0;     // two O accumulators (one per warpgroup) of d columns, 128 apart
+constexpr uint32_t kColS = 256;   // three S buffers of 64 columns; warpgroup h writes its P (32 bf16
+                                  // packed in 16 columns) over its own S columns [32h, 32h + 16)
+constexpr int kSBufs = 3;         // S is issued two tiles ahead of P.V
 // A row keeps a stale reference maximum until a tile's maximum exceeds it by this much (log2
 // units); then O and l are rescaled. The result is exact either way: O and l share the reference.
 constexpr float kRescaleLog2 = 8.0f;
@@ -58,20 +60,20 @@ struct Bars {
   uint64_t k_full[8];
   uint64_t v_full[8];
   uint64_t kv_empty[8];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_full;     // one phase per P.V MMA (the softmax waits on it before rescaling O)
+  uint64_t s_full[3];
+  uint64_t p_full[3][2];  // [S buffer][warpgroup]
+  uint64_t o_full[2][2];  // [warpgroup][tile parity]: one phase per P.V MMA of that parity (waited on
+                          // before rescaling O_h)
   uint64_t o_done;     // one phase, after the last P.V MMA (the epilogue waits on it)
   uint64_t q_ready;
   uint64_t drain;
-  uint64_t xchg[4];     // per lane quarter: the two warpgroups' half-tile maxima (one phase per tile)
-  uint64_t xchg_l[4];   // per lane quarter: the two halves of l at the end
+  uint64_t xchg_l[4];   // per lane quarter: the two halves' (m, l) at the end
   uint32_t tmem_base;
   int abort;
   int tile_base[8];     // per stage: what the mask needs of the tile in it (written by the producer
   int tile_valid[8];    // before it arrives on k_full, read by the consumers after waiting on it)
-  float xmax[2][2][128];  // [tile parity][warpgroup][TMEM lane]
-  float xl[2][128];       // [warpgroup][TMEM lane]
+  float xm[2][128];       // [warpgroup][TMEM lane]
+  float xl[2][128];
 };
 
 // The per-CTA work item.
@@ -215,17 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], kSoftmaxThreads);
+      mbar_init(&bars->p_full[i][0], kSoftmaxThreads / 2);
+      mbar_init(&bars->p_full[i][1], kSoftmaxThreads / 2);
     }
-    mbar_init(&bars->o_full, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->o_full[i >> 1][i & 1], 1);
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->q_ready, kSoftmaxThreads);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&bars->xchg[i], 64);
-      mbar_init(&bars->xchg_l[i], 64);
-    }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->xchg_l[i], 64);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -289,73 +289,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_ready, 0, abort, p.err));
     tc_fence_after();
     const uint32_t qaddr = smem_u32(sQ);
-    for (int j = 0; ok && j <= w.nt; ++j) {
-      if (j < w.nt) {
-        // S_j = Q K_j^T into S buffer j % 2
+    // S_j = Q K_j^T into S buffer j % 3, kept two tiles ahead of P.V: S_{jp+2} is issued before
+    // P.V of tile jp, as soon as the softmax of tile jp-1 has released buffer (jp+2) % 3.
+    int next_s = 0;
+    for (int jp = 0; ok && jp < w.nt; ++jp) {
+      while (next_s < w.nt && next_s <= jp + 2) {
+        const int j = next_s;
         const int st = j % C::kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (j / C::kStages) & 1, abort, p.err));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t kaddr = smem_u32(sK + st * C::kTileBytes);
-          const uint32_t d_s = tbase + kColS + (j & 1) * 64;
+          const uint32_t d_s = tbase + kColS + (j % kSBufs) * 64;
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint64_t a = sw128_desc(qaddr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024);
             const uint64_t bdesc = sw128_desc(kaddr + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
             mma_ss(d_s, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[j & 1]);
+          mma_commit(&bars->s_full[j % kSBufs]);
         }
         __syncwarp();
+        ++next_s;
       }
-      if (j >= 1) {
-        // O += P_{j-1} V_{j-1}
-        const int jp = j - 1;
-        const int st = jp % C::kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_full[jp & 1], (jp >> 1) & 1, abort, p.err));
-        if (!ok) break;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (jp / C::kStages) & 1, abort, p.err));
-        if (!ok) break;
-        // Keys outside every query's range may hold anything (stale ring slots, the unused tail
-        // of the last chunk). P is 0 there, but 0 * NaN is NaN on the tensor core, so their V rows
-        // are zeroed before the MMA reads them.
-        {
-          Tile t;
-          t.base = bars->tile_base[st];
-          t.valid = bars->tile_valid[st] != 0;
-          uint8_t* vt = sV + st * C::kTileBytes;
-          bool any = false;
-          for (int k = lane; k < kChunk; k += 32) {
-            int pos;
-            if (!key_in_union<RING>(p, w, t, k, &pos)) {
-              any = true;
+      if (!ok) break;
+      // O_h += P_h V_h for tile jp, h = 0 (keys 0..31) and 1 (keys 32..63)
+      const int st = jp % C::kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (jp / C::kStages) & 1, abort, p.err));
+      if (!ok) break;
+      // Keys outside every query's range may hold anything (stale ring slots, the unused tail of
+      // the last chunk). P is 0 there, but 0 * NaN is NaN on the tensor core, so their V rows are
+      // zeroed before the MMA reads them.
+      {
+        Tile t;
+        t.base = bars->tile_base[st];
+        t.valid = bars->tile_valid[st] != 0;
+        uint8_t* vt = sV + st * C::kTileBytes;
+        bool any = false;
+        for (int k = lane; k < kChunk; k += 32) {
+          int pos;
+          if (!key_in_union<RING>(p, w, t, k, &pos)) {
+            any = true;
 #pragma unroll
-              for (int bx = 0; bx < C::kBoxes; ++bx) {
-                uint4* row = reinterpret_cast<uint4*>(vt + bx * C::kBoxBytes + k * 128);
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+              uint4* row = reinterpret_cast<uint4*>(vt + bx * C::kBoxBytes + k * 128);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
-              }
+              for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
             }
           }
-          if (any) fence_proxy_async_smem();
-          __syncwarp();
         }
+        if (any) fence_proxy_async_smem();
+        __syncwarp();
+      }
+      const uint32_t vaddr = smem_u32(sV + st * C::kTileBytes);
+      const int sb = jp % kSBufs;
+      for (int h = 0; h < 2; ++h) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_full[sb][h], (jp / kSBufs) & 1, abort, p.err));
+        if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t vaddr = smem_u32(sV + st * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk) {
-            const uint64_t bdesc = sw128_desc(vaddr + kk * 2048, C::kBoxBytes, 1024);
-            mma_ts(tbase + kColO, tbase + kColP + (jp & 1) * 32 + kk * 8, bdesc, idesc_pv,
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t bdesc = sw128_desc(vaddr + (2 * h + kk) * 2048, C::kBoxBytes, 1024);
+            mma_ts(tbase + kColO + h * 128, tbase + kColS + sb * 64 + h * 32 + kk * 8, bdesc, idesc_pv,
                    (jp > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&bars->kv_empty[st]);
-          mma_commit(&bars->o_full);
-          if (jp == w.nt - 1) mma_commit(&bars->o_done);
+          mma_commit(&bars->o_full[h][jp & 1]);
         }
         __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(&bars->kv_empty[st]);
+        if (jp == w.nt - 1) mma_commit(&bars->o_done);
+      }
+      __syncwarp();
     }
     // Every MMA issued above completes before TMEM is freed.
     if (lane == 0) mma_commit(&bars->drain);
@@ -391,15 +400,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int p_i = w.L - w.nq + qi;                   // this row's query position
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const int k0 = wg * 32;                            // this warpgroup's first key in a tile
-    float m_ref = -INFINITY;                           // shared by both halves of the row
-    float l_half = 0.f;                                // this half's share of the row sum
+    const uint32_t col_o = kColO + wg * 128;           // this warpgroup's O accumulator
+    float m_ref = -INFINITY;                           // this half's reference maximum
+    float l_half = 0.f;                                // this half's row sum
     bool ok = true;
     for (int j = 0; j < w.nt; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort, p.err));
+      const int sb = j % kSBufs;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / kSBufs) & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[32];
-      tmem_ld32(lane_base + kColS + (j & 1) * 64 + k0, sr);
+      tmem_ld32(lane_base + kColS + sb * 64 + k0, sr);
       // The tile's geometry comes from the producer through shared memory (k_full has completed,
       // since S_j has: this wait only makes the producer's writes visible).
       const int st = j % C::kStages;
@@ -424,38 +435,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx[u] = fmaxf(fmaxf(sv[u], sv[u + 8]), fmaxf(sv[u + 16], sv[u + 24]));
-      const float half_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      // exchange the half maxima of the row with the other warpgroup
-      bars->xmax[j & 1][wg][mrow] = half_max;
-      mbar_arrive(&bars->xchg[quarter]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg[quarter], j & 1, abort, p.err));
-      if (!ok) break;
-      const float m_tile = fmaxf(half_max, bars->xmax[j & 1][wg ^ 1][mrow]) * p.scale_log2;
+      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
       bool need_o = false;
       float alpha = 1.f;
       if (m_tile > m_ref + kRescaleLog2) {
-        need_o = m_ref != -INFINITY;                  // O already holds weighted values
+        need_o = m_ref != -INFINITY;                  // O_h already holds weighted values
         alpha = ex2_approx(m_ref - m_tile);           // 0 when m_ref = -inf
         l_half *= alpha;
         m_ref = m_tile;
       }
       if (__any_sync(0xffffffffu, need_o)) {
-        // O holds the sum over tiles < j: wait for PV_{j-1}, then scale this warpgroup's half of
-        // the columns. S_j has completed, so PV_{j-2} has too; o_full is in phase j-1 or j, and the
-        // parity wait for phase j-1 is exact.
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full, (j - 1) & 1, abort, p.err));
+        // O_h holds the sum over tiles < j: wait for its P.V of tile j-1, then scale it. S_j has
+        // completed, so the P.V of tile j-3 has too, and P.V of tile j+1 needs this tile's P: the
+        // barrier of odd or even tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after,
+        // so the parity wait for phase (j-1)/2 is exact.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err));
         if (!ok) break;
         tc_fence_after();
         const float a = need_o ? alpha : 1.f;
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
-          const uint32_t col = kColO + wg * (HD / 2) + c * 32;
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_base + col, o);
+          tmem_ld32(lane_base + col_o + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-          tmem_st32(lane_base + col, o);
+          tmem_st32(lane_base + col_o + c * 32, o);
         }
       }
       // p = 2^(s * scale * log2e - m_ref); masked keys carry s = -inf and give exactly 0. A row that
@@ -472,18 +477,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       if (rv) l_half += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      tmem_st16(lane_base + kColP + (j & 1) * 32 + wg * 16, pk);
+      tmem_st16(lane_base + kColS + sb * 64 + k0, pk);    // P_h over this half's own S columns
       tc_fence_before();
-      mbar_arrive(&bars->p_full[j & 1]);
+      mbar_arrive(&bars->p_full[sb][wg]);
     }
-    // ---- epilogue: the split's partial (m, l, unnormalised O) ----
-    float l_sum = l_half;
+    // ---- epilogue: merge the two halves into the split's partial (m, l, unnormalised O) ----
+    float m_w[2] = {-INFINITY, -INFINITY}, l_w[2] = {0.f, 0.f};
     if (ok) {
+      bars->xm[wg][mrow] = l_half > 0.f ? m_ref : -INFINITY;
       bars->xl[wg][mrow] = l_half;
       mbar_arrive(&bars->xchg_l[quarter]);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg_l[quarter], 0, abort, p.err));
-      if (ok) l_sum = l_half + bars->xl[wg ^ 1][mrow];
+      if (ok) {
+        m_w[0] = bars->xm[0][mrow];
+        m_w[1] = bars->xm[1][mrow];
+        l_w[0] = bars->xl[0][mrow];
+        l_w[1] = bars->xl[1][mrow];
+      }
     }
+    const float m_row = fmaxf(m_w[0], m_w[1]);
+    const float w0 = l_w[0] > 0.f ? ex2_approx(m_w[0] - m_row) : 0.f;
+    const float w1 = l_w[1] > 0.f ? ex2_approx(m_w[1] - m_row) : 0.f;
+    const float l_sum = w0 * l_w[0] + w1 * l_w[1];
     // A parity wait on o_full cannot tell phase nt-1 from nt-3 when P.V_{nt-2} is still running,
     // so the last P.V has a barrier of its own.
     if (ok && w.nt > 0) {
@@ -491,24 +506,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if (ok) {
+      // warpgroup h writes columns [h d/2, (h + 1) d/2) of the merged O
       float* dst = p.part_o + (pidx * kMaxRows + r) * HD + wg * (HD / 2);
       if (w.nt > 0) {
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + kColO + wg * (HD / 2) + c * 32, o);
+          uint32_t o0[32], o1[32];
+          tmem_ld32(lane_base + kColO + wg * (HD / 2) + c * 32, o0);
+          tmem_ld32(lane_base + kColO + 128 + wg * (HD / 2) + c * 32, o1);
           if (rv && l_sum > 0.f) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               *reinterpret_cast<float4*>(dst + c * 32 + e) =
-                  make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
-                              __uint_as_float(o[e + 3]));
+                  make_float4(w0 * __uint_as_float(o0[e]) + w1 * __uint_as_float(o1[e]),
+                              w0 * __uint_as_float(o0[e + 1]) + w1 * __uint_as_float(o1[e + 1]),
+                              w0 * __uint_as_float(o0[e + 2]) + w1 * __uint_as_float(o1[e + 2]),
+                              w0 * __uint_as_float(o0[e + 3]) + w1 * __uint_as_float(o1[e + 3]));
           }
         }
       }
       if (rv && wg == 0) {
         float2* ml = reinterpret_cast<float2*>(p.part_ml) + pidx * kMaxRows + r;
-        *ml = make_float2(l_sum > 0.f ? m_ref : -INFINITY, l_sum);
+        *ml = make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum);
       }
     }
   }
