@@ -39,7 +39,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // two O accumulators (one per warpgroup) of d columns, 128 apart
 constexpr uint32_t kColS = 256;   // three S buffers of 64 columns; warpgroup h writes its P (32 bf16
                                   // packed in 16 columns) over its own S columns [32h, 32h + 16)
-constexpr int kSBufs = 3;         // S is issued two tiles ahead of P.V
+constexpr int kSBufs = 3;         // S is issued up to three tiles ahead of P.V
+constexpr int kPrefetch = 6;      // tiles prefetched into L2 beyond the shared-memory stages
 // A row keeps a stale reference maximum until a tile's maximum exceeds it by this much (log2
 // units); then O and l are rescaled. The result is exact either way: O and l share the reference.
 constexpr float kRescaleLog2 = 8.0f;
@@ -254,6 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ TMA producer -----------------------------------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
+      auto prefetch_tile = [&](int f) {
+        const Tile tf = tile_at<RING>(p, w, f);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_prefetch_2d(&tmap_k, bx * 64, tf.y);
+          tma_prefetch_2d(&tmap_v, bx * 64, tf.y);
+        }
+      };
       int issued = 0;
       bool reported = false;
       for (int j = 0; j < w.nt; ++j) {
@@ -274,6 +283,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
           tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &tmap_v, &bars->v_full[st], bx * 64, t.y, pol);
+        // Ask L2 for the tiles that follow the shared-memory stages, so that more of the stream is
+        // in flight from HBM than the stages alone can hold.
+        if (j == C::kStages - 1) {
+          for (int f = C::kStages; f < C::kStages + kPrefetch && f < w.nt; ++f) prefetch_tile(f);
+        } else if (j >= C::kStages && j + kPrefetch < w.nt) {
+          prefetch_tile(j + kPrefetch);
+        }
         issued = j + 1;
       }
       if (*abort) {
@@ -289,30 +305,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_ready, 0, abort, p.err));
     tc_fence_after();
     const uint32_t qaddr = smem_u32(sQ);
-    // S_j = Q K_j^T into S buffer j % 3, kept two tiles ahead of P.V: S_{jp+2} is issued before
-    // P.V of tile jp, as soon as the softmax of tile jp-1 has released buffer (jp+2) % 3.
+    // S_j = Q K_j^T into S buffer j % 3. Before P.V of tile jp, S of tiles up to jp is issued
+    // (waiting for their K if need be: the softmax of tile jp needs S_jp), and S of tiles up to
+    // jp + 2 only if their K has already landed, so that P.V never waits for a later tile's K and
+    // each stage is released as soon as its P.V completes. S_{jp+2} goes into the buffer that P.V
+    // of tile jp-1, issued before it, reads P from: MMAs run in issue order.
     int next_s = 0;
-    for (int jp = 0; ok && jp < w.nt; ++jp) {
-      while (next_s < w.nt && next_s <= jp + 2) {
-        const int j = next_s;
-        const int st = j % C::kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (j / C::kStages) & 1, abort, p.err));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t kaddr = smem_u32(sK + st * C::kTileBytes);
-          const uint32_t d_s = tbase + kColS + (j % kSBufs) * 64;
+    auto issue_s = [&](int j) {
+      const int st = j % C::kStages;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kaddr = smem_u32(sK + st * C::kTileBytes);
+        const uint32_t d_s = tbase + kColS + (j % kSBufs) * 64;
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint64_t a = sw128_desc(qaddr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bdesc = sw128_desc(kaddr + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
-            mma_ss(d_s, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->s_full[j % kSBufs]);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t a = sw128_desc(qaddr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bdesc = sw128_desc(kaddr + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+          mma_ss(d_s, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
         }
-        __syncwarp();
-        ++next_s;
+        mma_commit(&bars->s_full[j % kSBufs]);
       }
+      __syncwarp();
+    };
+    for (int jp = 0; ok && jp < w.nt; ++jp) {
+      while (ok && next_s <= jp) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[next_s % C::kStages], (next_s / C::kStages) & 1,
+                                               abort, p.err));
+        if (ok) issue_s(next_s++);
+      }
+      while (ok && next_s < w.nt && next_s <= jp + 2 &&
+             __all_sync(0xffffffffu, mbar_test_wait(&bars->k_full[next_s % C::kStages], (next_s / C::kStages) & 1)))
+        issue_s(next_s++);
       if (!ok) break;
       // O_h += P_h V_h for tile jp, h = 0 (keys 0..31) and 1 (keys 32..63)
       const int st = jp % C::kStages;
@@ -446,8 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_tile;
       }
       if (__any_sync(0xffffffffu, need_o)) {
-        // O_h holds the sum over tiles < j: wait for its P.V of tile j-1, then scale it. S_j has
-        // completed, so the P.V of tile j-3 has too, and P.V of tile j+1 needs this tile's P: the
+        // O_h holds the sum over tiles < j: wait for its P.V of tile j-1, then scale it. S_j was
+        // issued after P.V of tile j-3 (S_j needs the buffer it read) and has completed, so that
+        // P.V has too, and P.V of tile j+1 needs this tile's P: the
         // barrier of odd or even tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after,
         // so the parity wait for phase (j-1)/2 is exact.
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err));
