@@ -220,6 +220,32 @@ VFY_API vfy_status vfy_accept(vfy_ctx* ctx, const float* logits, int vocab, cons
                               int32_t* bonus, int32_t* committed, int num_seqs,
                               vfy_stream_t stream);
 
+/*
+ * vfy_accept_static -- vfy_accept for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point: it exists for integration. Some callers
+ * cannot call cudaMalloc: code running inside an allocator or memory pool it must not re-enter,
+ * plug-ins whose host owns every device allocation, and deployments whose device memory budget is
+ * fixed before decoding starts. vfy_accept needs a context, and vfy_create allocates; this call
+ * needs neither. Its scratch (argmax keys, a CTA ticket, an error word) is one fixed 8 KiB array in
+ * the library's device memory, held by every GPU that loads the library until the process exits.
+ *
+ * Arguments and results are those of vfy_accept, on the CURRENT device (`stream` must belong to
+ * it), with max_rows (a host bound on cu_rows[B]) at most 1024: a larger max_rows returns
+ * VFY_EINVAL and launches nothing. device_error (nullable) is a caller-owned device int32 that
+ * receives VFY device error bits (1 = out-of-range list, 2 = timeout) OR-ed in; the caller clears it.
+ *  - The first call on a device looks up the scratch array's device address
+ *    (cudaGetSymbolAddress) with that device current. Make that first call before any stream
+ *    capture.
+ *  - Each call clears the scratch on `stream` (cudaMemsetAsync) and then launches the kernel; it
+ *    calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Every call on a device shares the one array: calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race and give wrong results. Order them.
+ */
+VFY_API vfy_status vfy_accept_static(const float* logits, int vocab, const int32_t* drafts,
+                                     const int32_t* cu_rows, int num_seqs, int max_rows,
+                                     int32_t* accepted_len, int32_t* bonus, int32_t* committed,
+                                     int32_t* device_error, vfy_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,8 @@ from . import build as _build
 VFY_OK, VFY_EINVAL, VFY_ECUDA, VFY_ENOMEM, VFY_EUNSUPPORTED, VFY_EDEVICE_INPUT, VFY_EDEVICE_TIMEOUT = range(7)
 
 EXPORTS = ("vfy_create", "vfy_destroy", "vfy_get_status", "vfy_strerror", "vfy_set_splits",
-           "vfy_select_resident", "vfy_page_in", "vfy_attend_full", "vfy_attend_swa", "vfy_accept")
+           "vfy_select_resident", "vfy_page_in", "vfy_attend_full", "vfy_attend_swa", "vfy_accept",
+           "vfy_accept_static")
 
 
 class VfyError(RuntimeError):
@@ -60,6 +61,7 @@ def lib() -> ctypes.CDLL:
         L.vfy_attend_full.argtypes = [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P]
         L.vfy_attend_swa.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]
         L.vfy_accept.argtypes = [_P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _P]
+        L.vfy_accept_static.argtypes = [_P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P]
         for name in EXPORTS:
             if name not in ("vfy_destroy", "vfy_strerror"):
                 getattr(L, name).restype = _I
@@ -206,3 +208,14 @@ def vfy_accept(ctx: Context, logits, vocab: int, drafts, cu_rows, max_rows: int,
         ctx.handle, _dev(logits, F32, "logits"), vocab, _dev(drafts, I32, "drafts"), _dev(cu_rows, I32, "cu_rows"),
         max_rows, _dev(accepted_len, I32, "accepted_len"), _dev(bonus, I32, "bonus"),
         _dev(committed, I32, "committed"), num_seqs, _stream(stream)), "vfy_accept")
+
+
+def vfy_accept_static(logits, vocab: int, drafts, cu_rows, num_seqs: int, max_rows: int, accepted_len, bonus,
+                      committed, device_error=None, stream=None):
+    """vfy_accept without a context and without allocating (for callers that cannot allocate
+    device memory); max_rows <= 1024. See include/vfy.h."""
+    _check(lib().vfy_accept_static(
+        _dev(logits, F32, "logits"), vocab, _dev(drafts, I32, "drafts"), _dev(cu_rows, I32, "cu_rows"),
+        num_seqs, max_rows, _dev(accepted_len, I32, "accepted_len"), _dev(bonus, I32, "bonus"),
+        _dev(committed, I32, "committed"), _dev(device_error, I32, "device_error"), _stream(stream)),
+        "vfy_accept_static")
