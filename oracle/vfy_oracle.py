@@ -204,13 +204,15 @@ def softmax_attend(q, keys, values, scale: float):
 
 
 def attend_full_seq(q, k_pool, v_pool, resident_ids, resident_slots, seq_len: int,
-                    scale: float | None = None, return_rowsum: bool = False):
+                    scale: float | None = None, return_rowsum: bool = False, rows=None):
     """One sequence of a full-attention layer over the resident chunks of its KVFlash pool.
 
     q        bf16 bits [q][Hq][d]          the verify block's queries
     k_pool   bf16 bits [slots][Hkv][64][d] pool (v_pool alike)
     resident_ids, resident_slots           resident chunk indices and the slots holding them
     seq_len  L, including the q block tokens
+    rows     optional list of (query i, q-head g) to compute (the others are left NaN), for
+             samples of large cases
     Returns O [q][Hq][d] f64, LSE [q][Hq] f64 (and the softmax row sums if asked).
     """
     qf = bf16_to_f64(q)
@@ -229,15 +231,16 @@ def attend_full_seq(q, k_pool, v_pool, resident_ids, resident_slots, seq_len: in
     pos = np.concatenate(pos) if pos else np.zeros(0, dtype=np.int64)
     kk = np.concatenate(ks, axis=1) if ks else np.zeros((hkv, 0, d))
     vv = np.concatenate(vs, axis=1) if vs else np.zeros((hkv, 0, d))
-    out = np.zeros((nq, hq_count, d))
-    lse = np.zeros((nq, hq_count))
-    rsum = np.zeros((nq, hq_count))
-    for i in range(nq):
+    fill = np.nan if rows is not None else 0.0
+    out = np.full((nq, hq_count, d), fill)
+    lse = np.full((nq, hq_count), fill)
+    rsum = np.full((nq, hq_count), fill)
+    todo = rows if rows is not None else [(i, g) for i in range(nq) for g in range(hq_count)]
+    for i, g in todo:
         p_i = _query_position(seq_len, nq, i)
         sel = pos <= p_i
-        for g in range(hq_count):
-            h = _kv_head_of(g, group)
-            out[i, g], lse[i, g], rsum[i, g] = softmax_attend(qf[i, g], kk[h][sel], vv[h][sel], scale)
+        h = _kv_head_of(g, group)
+        out[i, g], lse[i, g], rsum[i, g] = softmax_attend(qf[i, g], kk[h][sel], vv[h][sel], scale)
     return (out, lse, rsum) if return_rowsum else (out, lse)
 
 

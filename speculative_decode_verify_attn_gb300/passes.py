@@ -4,7 +4,7 @@ The pass is the data-parallel hot path of one speculative-decoding step at long 
 ('Laguna XS 2.1 33B on a RTX 3090' (lucebox): 40 layers in a 3-in-4 window pattern, 'Three
 optimizations' items 1 and 3; CUDA-graph replay of the decode loop):
 
-  vfy_select_resident                       residency for this step (one chunk table for all
+  vfy_select_resident      (side stream)    residency for this step (one chunk table for all
                                             full layers; each full layer has its own pool)
   vfy_page_in x n_full      (side stream)   the step's newly resident chunks, host -> pools
   for layer l in 0..n_layers-1:             window layers where l % 4 != 3, full where l % 4 == 3
@@ -191,11 +191,13 @@ class VerifyPass:
         main = torch.cuda.current_stream(self.dev)
         events = {}
         if not self.all_resident:
-            vfy.vfy_select_resident(self.ctx, self.scores, self.cu_chunks, 1, self.n_chunks, self.k,
-                                    self.slot_of_chunk, self.res_ids, self.res_slots, self.cu_res,
-                                    self.pagein_list, self.pagein_count, main)
+            # Residency and page-in run on a side stream beside the window layers; each full layer
+            # waits for its own page-in (and so for the selection before it).
             self.side.wait_stream(main)
             with torch.cuda.stream(self.side):
+                vfy.vfy_select_resident(self.ctx, self.scores, self.cu_chunks, 1, self.n_chunks, self.k,
+                                        self.slot_of_chunk, self.res_ids, self.res_slots, self.cu_res,
+                                        self.pagein_list, self.pagein_count, self.side)
                 for l in self.full_layers:
                     vfy.vfy_page_in(self.ctx, self.host_k[l], self.host_v[l], self.n_chunks, self.pool_k[l],
                                     self.pool_v[l], self.k, self.pagein_list, self.pagein_count, 1, self.k,
