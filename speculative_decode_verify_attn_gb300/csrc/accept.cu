@@ -45,6 +45,7 @@ template <bool VEC4>
 __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) {
   __shared__ unsigned long long warp_best[kThreads / 32];
   __shared__ bool is_last;
+  pdl_launch_dependents();   // the next kernel may launch; it still waits for this grid
   pdl_wait();
   const int row = blockIdx.y;
   const int total_rows = p.cu_rows[p.num_seqs];
@@ -92,7 +93,6 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
   }
   __syncthreads();
   if (!is_last) {
-    pdl_launch_dependents();
     return;
   }
   __threadfence();
@@ -138,7 +138,6 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
   for (int r = threadIdx.x; r < p.max_rows; r += kThreads) p.keys[r] = 0ull;
   if (threadIdx.x == 0) *p.counter = 0u;
   __threadfence();
-  pdl_launch_dependents();
 }
 
 }  // namespace

@@ -243,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort = &bars->abort;
 
+  // Let the next kernel in the stream launch now: its prologue overlaps this kernel, and its
+  // griddepcontrol.wait still waits for this grid to complete.
+  pdl_launch_dependents();
   pdl_wait();
   const Work w = make_work<RING>(p);
   if (w.bad && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, kErrDeviceInput);
@@ -555,7 +558,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -579,6 +581,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   __shared__ float s_m[4];
   __shared__ float s_l[4];
   __shared__ float s_acc[4][HD];
+  pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = static_cast<int>(blockIdx.x / p.hq);
@@ -600,11 +603,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int nsub = min(kCombineMaxPerWarp, (p.num_splits - warp + 3) / 4);
   float2 my_ml = make_float2(-INFINITY, 0.f);
   if (lane < nsub) my_ml = __ldcg(ml + (p0 + warp + 4 * lane) * kMaxRows + r);
+  // The O rows are loaded in the same batch as (m, l): a split without data for this row may hold
+  // anything there, and its weight selects it out below (never multiplied in).
   Vec v[kCombineMaxPerWarp];
 #pragma unroll
   for (int u = 0; u < kCombineMaxPerWarp; ++u) {
-    const float l_u = __shfl_sync(0xffffffffu, my_ml.y, u);
-    if (u < nsub && l_u > 0.f)   // never read a split that holds no row data
+    if (u < nsub)
       v[u] = __ldcg(reinterpret_cast<const Vec*>(p.part_o + ((p0 + warp + 4 * u) * kMaxRows + r) * HD) + lane);
     else if constexpr (kPer == 4)
       v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -624,14 +628,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
 #pragma unroll
   for (int u = 0; u < kCombineMaxPerWarp; ++u) {
     const float wk = __shfl_sync(0xffffffffu, wgt, u);
+    const bool use = wk != 0.f;
     if constexpr (kPer == 4) {
-      acc[0] = fmaf(wk, v[u].x, acc[0]);
-      acc[1] = fmaf(wk, v[u].y, acc[1]);
-      acc[2] = fmaf(wk, v[u].z, acc[2]);
-      acc[3] = fmaf(wk, v[u].w, acc[3]);
+      acc[0] = use ? fmaf(wk, v[u].x, acc[0]) : acc[0];
+      acc[1] = use ? fmaf(wk, v[u].y, acc[1]) : acc[1];
+      acc[2] = use ? fmaf(wk, v[u].z, acc[2]) : acc[2];
+      acc[3] = use ? fmaf(wk, v[u].w, acc[3]) : acc[3];
     } else {
-      acc[0] = fmaf(wk, v[u].x, acc[0]);
-      acc[1] = fmaf(wk, v[u].y, acc[1]);
+      acc[0] = use ? fmaf(wk, v[u].x, acc[0]) : acc[0];
+      acc[1] = use ? fmaf(wk, v[u].y, acc[1]) : acc[1];
     }
   }
   if (lane == 0) {
@@ -675,7 +680,6 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     p.lse[static_cast<size_t>(t) * p.hq + hq] =
         lsum > 0.f ? (mmax + __log2f(lsum)) * 0.6931471805599453f : -INFINITY;
   }
-  pdl_launch_dependents();
 }
 
 }  // namespace

@@ -4,7 +4,9 @@
 // The device reads the host store directly (zero-copy over the host link), so the (chunk, slot)
 // list can stay in device memory and the copy can live inside a captured CUDA graph. Grid:
 // x = list entry (sequence b, entry i < k), y = part of the chunk; entries past pagein_count[b]
-// return at once. Each thread keeps 2 x 8 independent 16-byte loads in flight.
+// return at once. Each thread keeps 2 x 8 independent 16-byte loads in flight. The copy is bound by
+// the host link, not by the SMs: one CTA per chunk moves it about as fast as four, and the page-ins
+// that run beside the attention layers then take as few SMs from them as they can.
 #include "ptx.cuh"
 #include "vfy_internal.cuh"
 
@@ -12,7 +14,7 @@ namespace vfy {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kParts = 4;
+constexpr int kParts = 1;
 constexpr int kUnroll = 8;
 
 __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p) {
@@ -54,7 +56,6 @@ __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p)
       }
     }
   }
-  pdl_launch_dependents();
 }
 
 }  // namespace

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
   pdl_wait();
   const int b = blockIdx.x;
   const int k = p.k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c0 = p.cu_chunks[b];
   const int n = p.cu_chunks[b + 1] - c0;
   if (threadIdx.x == 0) {
@@ -85,7 +86,6 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
       p.pagein_count[b] = 0;
       if (b == 0) p.cu_res[0] = 0;
     }
-    pdl_launch_dependents();
     return;
   }
   const int kk = min(k, n);
@@ -108,26 +108,50 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
     for (int shift = 24; shift >= 0; shift -= 8) {
       if (threadIdx.x < 256) hist[threadIdx.x] = 0;
       __syncthreads();
-      for (int j = j0; j < j1; ++j) {
-        const uint32_t u = keys[j];
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+      // Lanes with the same digit add once per warp (the leading bytes of nearby scores agree,
+      // so plain atomics would queue on a few bins). `per` is the same for every thread.
+      for (int t = 0; t < per; ++t) {
+        const int j = j0 + t;
+        const bool valid = j < j1 && (keys[j] & mask) == prefix;
+        const uint32_t bin = valid ? (keys[j] >> shift) & 255u : 0xffffffffu;
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int above = 0;
-        int d = 255;
-        for (; d > 0; --d) {
-          if (above + hist[d] >= remaining) break;
-          above += hist[d];
+      if (warp == 0) {
+        // Lane l holds bins 255-8l .. 248-8l (descending). A scan over the lanes gives the count
+        // of keys in the bins above each lane's group; the lane whose group holds the
+        // remaining-th largest key finds the digit: the largest d whose bins >= d hold at least
+        // `remaining` keys (d = 255 when nothing remains to take).
+        int c[8];
+        int sum = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          c[u] = hist[255 - 8 * lane - u];
+          sum += c[u];
         }
-        s_remaining = remaining - above;
-        s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int above_group = incl - sum;
+        if ((remaining <= 0 && lane == 0) || (above_group < remaining && remaining <= incl)) {
+          int above = above_group;
+          int u = 0;
+          for (; u < 7; ++u) {
+            if (above + c[u] >= remaining) break;
+            above += c[u];
+          }
+          s_remaining = remaining - above;
+          s_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - u) << shift);
+        }
       }
       __syncthreads();
       remaining = s_remaining;
       prefix = s_prefix;
       mask |= 255u << shift;
-      __syncthreads();
     }
     thr = prefix;
     take_eq = remaining;
@@ -230,7 +254,6 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
     p.pagein_count[b] = tot_new;
     if (s_flag) atomicOr(p.err, kErrDeviceInput);
   }
-  pdl_launch_dependents();
 }
 
 }  // namespace

@@ -128,7 +128,8 @@ class VerifyPass:
         self.accepted = torch.zeros(1, dtype=torch.int32, device=dev)
         self.bonus = torch.zeros(1, dtype=torch.int32, device=dev)
         self.committed = torch.zeros(self.q, dtype=torch.int32, device=dev)
-        self.side = torch.cuda.Stream(device=dev)
+        # Paging gets the higher priority: its CTAs go ahead of queued layer CTAs as SMs free up.
+        self.side = torch.cuda.Stream(device=dev, priority=-1)
         self.graph = None
         self.step = 0
 
