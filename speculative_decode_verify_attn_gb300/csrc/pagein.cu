@@ -4,9 +4,10 @@
 // The device reads the host store directly (zero-copy over the host link), so the (chunk, slot)
 // list can stay in device memory and the copy can live inside a captured CUDA graph. Grid:
 // x = list entry (sequence b, entry i < k), y = part of the chunk; entries past pagein_count[b]
-// return at once. Each thread keeps 2 x 8 independent 16-byte loads in flight. The copy is bound by
-// the host link, not by the SMs: one CTA per chunk moves it about as fast as four, and the page-ins
-// that run beside the attention layers then take as few SMs from them as they can.
+// return at once. Each thread keeps 2 x 2 independent 16-byte loads in flight. The copy is bound by
+// the host link, which a quarter of a megabyte in flight already fills (16 chunks x 256 threads x 4
+// loads); more outstanding host reads only queue in the memory system and slow the attention
+// kernels running beside the page-in, and so do more CTAs.
 #include "ptx.cuh"
 #include "vfy_internal.cuh"
 
@@ -15,7 +16,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kParts = 1;
-constexpr int kUnroll = 8;
+constexpr int kUnroll = 2;
 
 __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p) {
   pdl_wait();

@@ -32,6 +32,23 @@ def is_full_layer(layer: int) -> bool:
     return layer % 4 == 3
 
 
+def join_points(n_full: int) -> dict[int, int]:
+    """Where the layer chain waits for the paging stream: {full layer j: last page-in it waits for}.
+
+    Page-ins complete in order on one stream, so waiting for page-in m covers every page-in up to
+    m. Full layer j joins up to page-in min(2j, n_full - 1) unless an earlier join already covered
+    page-in j: joins at j = 0, 1, 3, 7, ... with groups of 1, 2, 4, 8, ... page-ins. Each group is
+    due well after it completes (a full layer comes every four layers, while a page-in takes about
+    as long as one layer), and every full layer j still waits for its own page-in j.
+    """
+    joins, covered = {}, -1
+    for j in range(n_full):
+        if j > covered:
+            covered = min(2 * j, n_full - 1)
+            joins[j] = covered
+    return joins
+
+
 @dataclass
 class PassSizes:
     n_layers: int
@@ -191,9 +208,12 @@ class VerifyPass:
         """Enqueue one pass on the current stream (used for capture and for eager runs)."""
         main = torch.cuda.current_stream(self.dev)
         events = {}
+        joins = {}
         if not self.all_resident:
-            # Residency and page-in run on a side stream beside the window layers; each full layer
-            # waits for its own page-in (and so for the selection before it).
+            # Residency and page-in run on a side stream beside the window layers. A full layer
+            # must not start before its own page-in, but every cross-stream wait in the layer
+            # chain costs the overlap of one kernel launch, so the chain joins the side stream
+            # only at the full layers join_points() names, each time for a group of page-ins.
             self.side.wait_stream(main)
             with torch.cuda.stream(self.side):
                 vfy.vfy_select_resident(self.ctx, self.scores, self.cu_chunks, 1, self.n_chunks, self.k,
@@ -206,11 +226,14 @@ class VerifyPass:
                     ev = torch.cuda.Event()
                     ev.record(self.side)
                     events[l] = ev
+            joins = join_points(len(self.full_layers))
+        fi = 0
         for l in range(self.n_layers):
             if is_full_layer(l):
-                if l in events:
-                    main.wait_event(events[l])
+                if fi in joins:
+                    main.wait_event(events[self.full_layers[joins[fi]]])
                 self.attend_full_layer(l, main)
+                fi += 1
             else:
                 self.attend_swa_layer(l, main)
         vfy.vfy_accept(self.ctx, self.logits, self.vocab, self.drafts, self.cu_rows, self.q, self.accepted,
