@@ -338,8 +338,15 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   p.part_o = ctx->part_o;
   p.part_ml = ctx->part_ml;
   p.err = ctx->err;
+  // Up to kMaxClusterSplits splits (and no more than one GPC holds) merge inside the attention
+  // kernel, as one thread-block cluster per (sequence, KV head); more go through the combine.
+  const bool merge = splits <= vfy::kMaxClusterSplits && splits <= vfy::attend_merge_limit(ring, c.head_dim);
+  p.out = merge ? out : nullptr;
+  p.lse = merge ? lse : nullptr;
+  p.token_cap = num_seqs * c.max_queries_per_seq;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  VFY_CUDA(vfy::launch_attend(ring, c.head_dim, p, tk, tv, num_seqs, s));
+  VFY_CUDA(vfy::launch_attend(ring, c.head_dim, merge, p, tk, tv, num_seqs, s));
+  if (merge) return VFY_OK;
 
   vfy::CombineParams cp;
   cp.cu_q = cu_q;

@@ -45,16 +45,25 @@ constexpr int kPrefetch = 6;      // tiles prefetched into L2 beyond the shared-
 // units); then O and l are rescaled. The result is exact either way: O and l share the reference.
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int HD>
+// MERGE: the splits of one (b, h) form a cluster and merge in the kernel. Every CTA then keeps a
+// receive area where the other splits store their partial rows: for the block rows it owns (rows
+// rank, rank + n, ...; slot k holds row rank + n k) one (m, l) pair and one fp32 O row per split,
+// at index k * n + split. k * n + split < kMaxRows + n, so kMaxRows + kMaxClusterSplits entries
+// cover every cluster size. A merging CTA processes few tiles, so it takes fewer K/V stages.
+template <int HD, bool MERGE>
 struct Cfg {
   static constexpr int kBoxes = HD / 64;               // 128-byte (64-column) boxes per row
   static constexpr int kBoxBytes = kChunk * 128;       // one 64-row box
   static constexpr int kQBoxBytes = kMaxRows * 128;
   static constexpr int kQBytes = kMaxRows * HD * 2;
   static constexpr int kTileBytes = kChunk * HD * 2;
-  static constexpr int kStages = HD == 128 ? 5 : 8;
-  static constexpr int kBarOffset = kQBytes + 2 * kStages * kTileBytes;
+  static constexpr int kStages = HD == 128 ? (MERGE ? 3 : 5) : 8;
+  static constexpr int kRecvEntries = kMaxRows + kMaxClusterSplits;
+  static constexpr int kRecvOffset = kQBytes + 2 * kStages * kTileBytes;
+  static constexpr int kRecvMlOffset = kRecvOffset + (MERGE ? kRecvEntries * HD * 4 : 0);
+  static constexpr int kBarOffset = kRecvMlOffset + (MERGE ? kRecvEntries * 8 : 0);
   static constexpr int kSmemBytes = kBarOffset + 4096 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct Bars {
@@ -75,7 +84,9 @@ struct Bars {
   int tile_valid[8];    // before it arrives on k_full, read by the consumers after waiting on it)
   float xm[2][128];       // [warpgroup][TMEM lane]
   float xl[2][128];
+  float2 sml[128];        // cluster merge: this split's (m, l) per block row
 };
+static_assert(sizeof(Bars) <= 4096, "barrier block overflows its reservation");
 
 // The per-CTA work item.
 struct Work {
@@ -196,11 +207,21 @@ __device__ __forceinline__ void key_interval(const AttnParams& p, const Work& w,
   }
 }
 
-template <int HD, bool RING>
+// Cluster merge: a split first stages its merged O rows in its own (then idle) K/V stages, fp32,
+// row r at r * HD floats with 16-byte chunk c at chunk c ^ ((r >> 2) & 7): the softmax lanes of a
+// warp hold rows 4 apart and write without bank conflicts, and a warp reading one row sees a
+// permutation of its chunks.
+template <int HD>
+__device__ __forceinline__ uint32_t staged_offset(int r, int col) {
+  const int c = col >> 2;
+  return static_cast<uint32_t>((r * HD + ((c ^ ((r >> 2) & 7)) << 2) + (col & 3)) * 4);
+}
+
+template <int HD, bool RING, bool MERGE>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, MERGE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -532,7 +553,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort, p.err));
       tc_fence_after();
     }
-    if (ok) {
+    if constexpr (MERGE) {
+      // Stage the split's (m, l, unnormalised O) rows locally; a split without data for a row
+      // stages (-inf, 0) and no O. Then every softmax warp forwards whole rows, one 512-byte store
+      // per row (d = 128), into the receive area of the row's owner, split rank r % n.
+      uint8_t* so = sK;                                // the K and V stages, idle after o_done
+      if (ok && w.nt > 0) {
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(lane_base + kColO + wg * (HD / 2) + c * 32, o0);
+          tmem_ld32(lane_base + kColO + 128 + wg * (HD / 2) + c * 32, o1);
+          if (rv && l_sum > 0.f) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              *reinterpret_cast<float4*>(so + staged_offset<HD>(r, wg * (HD / 2) + c * 32 + x)) =
+                  make_float4(w0 * __uint_as_float(o0[x]) + w1 * __uint_as_float(o1[x]),
+                              w0 * __uint_as_float(o0[x + 1]) + w1 * __uint_as_float(o1[x + 1]),
+                              w0 * __uint_as_float(o0[x + 2]) + w1 * __uint_as_float(o1[x + 2]),
+                              w0 * __uint_as_float(o0[x + 3]) + w1 * __uint_as_float(o1[x + 3]));
+          }
+        }
+      }
+      if (wg == 0) bars->sml[r] = make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum);
+      named_bar_sync(1, kSoftmaxThreads);
+      const int n = static_cast<int>(cluster_nctarank());
+      const int rank = static_cast<int>(cluster_ctarank());
+      constexpr int kPer = HD / 32;
+      const uint32_t recv = smem_u32(smem + C::kRecvOffset);
+      const uint32_t recv_ml = smem_u32(smem + C::kRecvMlOffset);
+      for (int rr = warp; rr < w.rows; rr += kSoftmaxThreads / 32) {
+        const float2 ml = bars->sml[rr];
+        const int e = (rr / n) * n + rank;             // entry in the owner's receive area
+        const uint32_t owner = static_cast<uint32_t>(rr % n);
+        if (lane == 0) st_dsmem_f2(dsmem_addr(recv_ml + e * 8, owner), ml);
+        if (ml.y > 0.f) {
+          const uint32_t dst = dsmem_addr(recv + (e * HD + lane * kPer) * 4, owner);
+          if constexpr (kPer == 4)
+            st_dsmem_f4(dst, *reinterpret_cast<const float4*>(so + staged_offset<HD>(rr, lane * 4)));
+          else
+            st_dsmem_f2(dst, *reinterpret_cast<const float2*>(so + staged_offset<HD>(rr, lane * 2)));
+        }
+      }
+    } else if (ok) {
       // warpgroup h writes columns [h d/2, (h + 1) d/2) of the merged O
       float* dst = p.part_o + (pidx * kMaxRows + r) * HD + wg * (HD / 2);
       if (w.nt > 0) {
@@ -555,6 +618,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (rv && wg == 0) {
         float2* ml = reinterpret_cast<float2*>(p.part_ml) + pidx * kMaxRows + r;
         *ml = make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum);
+      }
+    }
+  }
+  if constexpr (MERGE) {
+    // ---- cluster merge: the CTAs of the cluster are the splits of this (b, h), in rank order.
+    // After the barrier every owner holds, in its own shared memory, all splits' (m, l, o) of its
+    // rows rank + n k; one warp merges one row and writes its bf16 output and log-sum-exp:
+    //   O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  LSE = ln2 * (M + log2 sum_s 2^(m_s - M) l_s)
+    // No CTA touches another's shared memory after the barrier, so each exits when done.
+    __syncwarp();
+    cluster_sync_all();
+    const int n = static_cast<int>(cluster_nctarank());
+    const int rank = static_cast<int>(cluster_ctarank());
+    constexpr int kPer = HD / 32;                      // columns per lane
+    const float* recv = reinterpret_cast<const float*>(smem + C::kRecvOffset);
+    const float2* recv_ml = reinterpret_cast<const float2*>(smem + C::kRecvMlOffset);
+    for (int k = warp;; k += kThreads / 32) {
+      const int r = rank + n * k;
+      if (r >= w.rows) break;
+      const float2 ml = lane < n ? recv_ml[k * n + lane] : make_float2(-INFINITY, 0.f);
+      float mm = ml.y > 0.f ? ml.x : -INFINITY;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+      const float wgt = ml.y > 0.f ? ex2_approx(ml.x - mm) : 0.f;
+      float lsum = wgt * ml.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+      float acc[kPer];
+#pragma unroll
+      for (int x = 0; x < kPer; ++x) acc[x] = 0.f;
+      for (int s = 0; s < n; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, wgt, s);
+        if (ws == 0.f) continue;                       // a split without data sent no O row
+        const float* src = recv + static_cast<size_t>(k * n + s) * HD + lane * kPer;
+        if constexpr (kPer == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] = fmaf(ws, v.x, acc[0]);
+          acc[1] = fmaf(ws, v.y, acc[1]);
+          acc[2] = fmaf(ws, v.z, acc[2]);
+          acc[3] = fmaf(ws, v.w, acc[3]);
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          acc[0] = fmaf(ws, v.x, acc[0]);
+          acc[1] = fmaf(ws, v.y, acc[1]);
+        }
+      }
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const int t = w.q0 + r / p.group;
+      const int hq = w.h * p.group + r % p.group;
+      if (t < p.token_cap) {
+        uint16_t* dst = p.out + (static_cast<size_t>(t) * p.hq + hq) * HD + lane * kPer;
+        if constexpr (kPer == 4) {
+          const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+          const __nv_bfloat162 c = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+          uint2 w2;
+          w2.x = *reinterpret_cast<const uint32_t*>(&a);
+          w2.y = *reinterpret_cast<const uint32_t*>(&c);
+          *reinterpret_cast<uint2*>(dst) = w2;
+        } else {
+          const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+          *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&a);
+        }
+        if (p.lse != nullptr && lane == 0)
+          p.lse[static_cast<size_t>(t) * p.hq + hq] =
+              lsum > 0.f ? (mm + __log2f(lsum)) * 0.6931471805599453f : -INFINITY;
       }
     }
   }
@@ -684,24 +812,67 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
 
 }  // namespace
 
+// Largest cluster of attend_kernel<HD, RING, true> CTAs that can be resident on the current
+// device (one CTA per SM: the cluster must fit in one GPC), cached per device.
 template <int HD, bool RING>
+static int merge_cluster_limit() {
+  static int limit[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (limit[dev] != 0) return limit[dev];
+  auto kern = attend_kernel<HD, RING, true>;
+  static size_t done[64] = {};
+  if (ensure_smem_limit(kern, Cfg<HD, true>::kSmemBytes, done) != cudaSuccess) return 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kMaxClusterSplits, 1, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<HD, true>::kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxPotentialClusterSize(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  limit[dev] = n < 1 ? 1 : (n > kMaxClusterSplits ? kMaxClusterSplits : n);
+  return limit[dev];
+}
+
+template <int HD, bool RING, bool MERGE>
 static cudaError_t launch_attend_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                    int num_seqs, cudaStream_t stream) {
   static size_t done[64] = {};
-  auto kern = attend_kernel<HD, RING>;
-  cudaError_t e = ensure_smem_limit(kern, Cfg<HD>::kSmemBytes, done);
+  auto kern = attend_kernel<HD, RING, MERGE>;
+  constexpr int kSmem = Cfg<HD, MERGE>::kSmemBytes;
+  cudaError_t e = ensure_smem_limit(kern, kSmem, done);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_splits, p.hkv, num_seqs);
-  return launch_pdl(kern, grid, dim3(kThreads), Cfg<HD>::kSmemBytes, stream, p, tk, tv);
+  if constexpr (!MERGE) {
+    return launch_pdl(kern, grid, dim3(kThreads), kSmem, stream, p, tk, tv);
+  } else {
+    if (p.num_splits > merge_cluster_limit<HD, RING>()) return cudaErrorNotSupported;
+    return launch_pdl_cluster(kern, grid, dim3(kThreads), kSmem, p.num_splits, stream, p, tk, tv);
+  }
 }
 
-cudaError_t launch_attend(bool ring, int head_dim, const AttnParams& p, const CUtensorMap& tk,
+int attend_merge_limit(bool ring, int head_dim) {
+  if (head_dim == 128) return ring ? merge_cluster_limit<128, true>() : merge_cluster_limit<128, false>();
+  return ring ? merge_cluster_limit<64, true>() : merge_cluster_limit<64, false>();
+}
+
+cudaError_t launch_attend(bool ring, int head_dim, bool merge, const AttnParams& p, const CUtensorMap& tk,
                           const CUtensorMap& tv, int num_seqs, cudaStream_t stream) {
+  if (merge) {
+    if (head_dim == 128)
+      return ring ? launch_attend_t<128, true, true>(p, tk, tv, num_seqs, stream)
+                  : launch_attend_t<128, false, true>(p, tk, tv, num_seqs, stream);
+    return ring ? launch_attend_t<64, true, true>(p, tk, tv, num_seqs, stream)
+                : launch_attend_t<64, false, true>(p, tk, tv, num_seqs, stream);
+  }
   if (head_dim == 128)
-    return ring ? launch_attend_t<128, true>(p, tk, tv, num_seqs, stream)
-                : launch_attend_t<128, false>(p, tk, tv, num_seqs, stream);
-  return ring ? launch_attend_t<64, true>(p, tk, tv, num_seqs, stream)
-              : launch_attend_t<64, false>(p, tk, tv, num_seqs, stream);
+    return ring ? launch_attend_t<128, true, false>(p, tk, tv, num_seqs, stream)
+                : launch_attend_t<128, false, false>(p, tk, tv, num_seqs, stream);
+  return ring ? launch_attend_t<64, true, false>(p, tk, tv, num_seqs, stream)
+              : launch_attend_t<64, false, false>(p, tk, tv, num_seqs, stream);
 }
 
 cudaError_t launch_combine(int head_dim, const CombineParams& p, cudaStream_t stream) {

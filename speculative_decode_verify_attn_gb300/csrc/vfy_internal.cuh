@@ -37,8 +37,16 @@ struct AttnParams {
   // split partials (workspace)
   float* part_o;              // [B][Hkv][splits][128][d]
   float* part_ml;             // [B][Hkv][splits][128][2] (m in log2 units, l)
+  // cluster-merged launches only: the splits of one (b, h) merge in the kernel and write these
+  uint16_t* out;              // [T][Hq][d]
+  float* lse;                 // [T][Hq] or null
+  int token_cap;              // host bound on cu_q[B]
   int* err;
 };
+
+// Splits of one (sequence, KV head) that one cluster can merge in the attention kernel (the
+// largest non-portable cluster).
+constexpr int kMaxClusterSplits = 16;
 
 struct CombineParams {
   const int32_t* cu_q;
@@ -55,9 +63,14 @@ struct CombineParams {
   int* err;
 };
 
-cudaError_t launch_attend(bool ring, int head_dim, const AttnParams& p, const CUtensorMap& tk,
-                          const CUtensorMap& tv, int num_seqs, cudaStream_t stream);
+// merge_in_cluster: the grid's x dimension (the splits) is one cluster, which merges the splits
+// and writes p.out / p.lse itself (no combine launch follows). Returns cudaErrorNotSupported,
+// before launching anything, when such a cluster cannot be resident on this device.
+cudaError_t launch_attend(bool ring, int head_dim, bool merge_in_cluster, const AttnParams& p,
+                          const CUtensorMap& tk, const CUtensorMap& tv, int num_seqs, cudaStream_t stream);
 cudaError_t launch_combine(int head_dim, const CombineParams& p, cudaStream_t stream);
+// The most splits one merging launch can take on the current device (0 on error).
+int attend_merge_limit(bool ring, int head_dim);
 
 // ------------------------------ acceptance --------------------------------------------------
 struct AcceptParams {
@@ -127,6 +140,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// launch_pdl with the grid's x dimension split into clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster_x,
+                               cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

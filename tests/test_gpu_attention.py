@@ -226,7 +226,9 @@ def test_swa_32k_wrapping(H, vfy):
     assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
 
 
-@pytest.mark.parametrize("splits", [1, 2, 5, 10])
+# Up to 16 splits merge inside the attention kernel (one cluster per KV head); 17 and 40 go through
+# the combine kernel. 16 and 40 leave some splits without a tile.
+@pytest.mark.parametrize("splits", [1, 2, 5, 10, 16, 17, 40])
 @pytest.mark.parametrize("phi", [0, 63, 64, 1500, 2047])
 def test_swa_offsets_and_splits(H, vfy, phi, splits):
     rng = np.random.default_rng(11 + phi)
@@ -236,9 +238,11 @@ def test_swa_offsets_and_splits(H, vfy, phi, splits):
     qb = synth.normal_bf16(rng, (q, s.num_q_heads, s.head_dim))
     ctx = make_ctx(vfy, s)
     vfy.vfy_set_splits(ctx, 0, splits)
-    got, _ = H.attend_swa(ctx, qb, [0, q], rk, rv, [phi], [L])
-    ref, _ = O.attend_ring_seq(qb, rk[0], rv[0], phi, L, 512)
+    got, lse = H.attend_swa(ctx, qb, [0, q], rk, rv, [phi], [L])
+    ref, rlse = O.attend_ring_seq(qb, rk[0], rv[0], phi, L, 512)
     assert_attn_close(got, ref, f"phi={phi} splits={splits}")
+    assert_lse_close(lse, rlse, f"phi={phi} splits={splits}")
+    assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
 
 
 @pytest.mark.parametrize("L", [1, 17, 100, 511, 512, 528, 529, 2000])
