@@ -340,12 +340,15 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   p.err = ctx->err;
   // Up to kMaxClusterSplits splits (and no more than one GPC holds) merge inside the attention
   // kernel, as one thread-block cluster per (sequence, KV head); more go through the combine.
+  // Full-layer splits over many resident chunks take wide tiles.
   const bool merge = splits <= vfy::kMaxClusterSplits && splits <= vfy::attend_merge_limit(ring, c.head_dim);
+  const bool wide = !ring && !merge && ceil_div(max_res, splits) >= vfy::kWideMinChunks;
+  const vfy::AttnTiles tiles = merge ? vfy::AttnTiles::kMerge : (wide ? vfy::AttnTiles::kWide : vfy::AttnTiles::kNarrow);
   p.out = merge ? out : nullptr;
   p.lse = merge ? lse : nullptr;
   p.token_cap = num_seqs * c.max_queries_per_seq;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  VFY_CUDA(vfy::launch_attend(ring, c.head_dim, merge, p, tk, tv, num_seqs, s));
+  VFY_CUDA(vfy::launch_attend(ring, c.head_dim, tiles, p, tk, tv, num_seqs, s));
   if (merge) return VFY_OK;
 
   vfy::CombineParams cp;

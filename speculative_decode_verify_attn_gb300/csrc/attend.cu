@@ -13,12 +13,16 @@
 //
 // One CTA handles one (sequence b, KV head h, split s): a contiguous run of tiles. Warp roles:
 //   warps 0-7  load Q, then the masked online softmax and the epilogue. Warps w and w + 4 share
-//              TMEM lane quarter w % 4 (one row per lane); warpgroup h takes keys [32h, 32h + 32)
-//              of every 64-key tile and keeps its own running maximum, row sum and O accumulator
-//              (O_h += P_h V_h, a K = 32 MMA), so the two halves never wait on each other; they
-//              are merged once, in the epilogue.
-//   warp 8     TMA producer (K and V tiles into a ring of smem stages)
-//   warp 9     TMEM owner and MMA issuer (one elected lane)
+//              TMEM lane quarter w % 4 (one row per lane); warpgroup h takes the second or first
+//              half of every tile's keys and keeps its own running maximum, row sum and O
+//              accumulator (O_h += P_h V_h), so the two halves never wait on each other; they are
+//              merged once, in the epilogue. A tile is two 64-token chunks (one per warpgroup) in
+//              full layers and one chunk (32 keys per warpgroup) in window layers and in merging
+//              launches, which are latency-bound.
+//   warp 8     TMA producer of K tiles (a ring of smem stages, released when S has read them) and
+//              of the tile geometry the softmax needs (a ring of its own)
+//   warp 9     TMEM owner and MMA issuer (one lane)
+//   warp 10    TMA producer of V tiles (a ring released when P.V has read them)
 // Row r = i * G + g (query i, q-head g of the group) sits in TMEM lane (r % 4) * 32 + r / 4, so the
 // real rows spread over the four lane quarters and all four softmax warps share the work.
 #include <cuda_bf16.h>
@@ -31,15 +35,16 @@
 namespace vfy {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;
+constexpr int kGeo = 16;          // tile-geometry ring: at least the K stages plus the S buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // two O accumulators (one per warpgroup) of d columns, 128 apart
-constexpr uint32_t kColS = 256;   // three S buffers of 64 columns; warpgroup h writes its P (32 bf16
-                                  // packed in 16 columns) over its own S columns [32h, 32h + 16)
-constexpr int kSBufs = 3;         // S is issued up to three tiles ahead of P.V
+constexpr uint32_t kColS = 256;   // S buffers of one column per key; warpgroup h writes its P (bf16,
+                                  // two per column) over the first half of its own S columns
 constexpr int kPrefetch = 6;      // tiles prefetched into L2 beyond the shared-memory stages
 // A row keeps a stale reference maximum until a tile's maximum exceeds it by this much (log2
 // units); then O and l are rescaled. The result is exact either way: O and l share the reference.
@@ -50,16 +55,28 @@ constexpr float kRescaleLog2 = 8.0f;
 // rank, rank + n, ...; slot k holds row rank + n k) one (m, l) pair and one fp32 O row per split,
 // at index k * n + split. k * n + split < kMaxRows + n, so kMaxRows + kMaxClusterSplits entries
 // cover every cluster size. A merging CTA processes few tiles, so it takes fewer K/V stages.
-template <int HD, bool MERGE>
+template <int HD, bool RING, bool MERGE, bool WIDE>
 struct Cfg {
+  static_assert(!WIDE || (!RING && !MERGE), "wide tiles are for full layers without the cluster merge");
+  static constexpr int kCPT = WIDE ? 2 : 1;             // 64-token chunks per tile
+  static constexpr int kKT = kCPT * kChunk;             // keys per tile
+  static constexpr int kKH = kKT / 2;                   // keys per warpgroup half
+  static constexpr int kSBufs = kCPT == 2 ? 2 : 3;      // S issued up to kSBufs - 1 tiles ahead
   static constexpr int kBoxes = HD / 64;               // 128-byte (64-column) boxes per row
-  static constexpr int kBoxBytes = kChunk * 128;       // one 64-row box
+  static constexpr int kBoxBytes = kKT * 128;          // one box: a tile's rows, 128 bytes each
+  static constexpr int kChunkRowsBytes = kChunk * 128; // one chunk's rows within a box
   static constexpr int kQBoxBytes = kMaxRows * 128;
   static constexpr int kQBytes = kMaxRows * HD * 2;
-  static constexpr int kTileBytes = kChunk * HD * 2;
-  static constexpr int kStages = HD == 128 ? (MERGE ? 3 : 5) : 8;
+  static constexpr int kTileBytes = kKT * HD * 2;
+  static constexpr int kChunkBytes = kChunk * HD * 2;
+  // K and V stage rings. A K stage frees when S has read it, a V stage only after P.V, so the K
+  // ring runs further ahead.
+  static constexpr int kKStages = WIDE ? (HD == 128 ? 3 : 5) : (HD == 128 ? (MERGE ? 3 : 6) : 8);
+  static constexpr int kVStages = WIDE ? (HD == 128 ? 2 : 4) : (HD == 128 ? (MERGE ? 3 : 5) : 8);
+  static_assert(kKStages <= 8 && kVStages <= 8 && kKStages + kSBufs <= kGeo, "rings");
+  static_assert(kColS + kSBufs * kKT <= kTmemCols, "tensor memory");
   static constexpr int kRecvEntries = kMaxRows + kMaxClusterSplits;
-  static constexpr int kRecvOffset = kQBytes + 2 * kStages * kTileBytes;
+  static constexpr int kRecvOffset = kQBytes + (kKStages + kVStages) * kTileBytes;
   static constexpr int kRecvMlOffset = kRecvOffset + (MERGE ? kRecvEntries * HD * 4 : 0);
   static constexpr int kBarOffset = kRecvMlOffset + (MERGE ? kRecvEntries * 8 : 0);
   static constexpr int kSmemBytes = kBarOffset + 4096 + 1024;
@@ -69,7 +86,9 @@ struct Cfg {
 struct Bars {
   uint64_t k_full[8];
   uint64_t v_full[8];
-  uint64_t kv_empty[8];
+  uint64_t k_empty[8];
+  uint64_t v_empty[8];
+  uint64_t geo_full[kGeo];  // tile j's geometry is in entry j % kGeo
   uint64_t s_full[3];
   uint64_t p_full[3][2];  // [S buffer][warpgroup]
   uint64_t o_full[2][2];  // [warpgroup][tile parity]: one phase per P.V MMA of that parity (waited on
@@ -80,8 +99,9 @@ struct Bars {
   uint64_t xchg_l[4];   // per lane quarter: the two halves' (m, l) at the end
   uint32_t tmem_base;
   int abort;
-  int tile_base[8];     // per stage: what the mask needs of the tile in it (written by the producer
-  int tile_valid[8];    // before it arrives on k_full, read by the consumers after waiting on it)
+  int tile_base[kGeo][2];  // per tile (j % kGeo) and chunk: what the mask needs (written by the K
+  int tile_valid[kGeo][2]; // producer before it arrives on geo_full, read by the softmax after)
+  int tile_zero[kGeo];     // some key of the tile lies outside every query's range
   float xm[2][128];       // [warpgroup][TMEM lane]
   float xl[2][128];
   float2 sml[128];        // cluster merge: this split's (m, l) per block row
@@ -95,12 +115,13 @@ struct Work {
   int L;
   int tb, nt;      // first tile (index within the (b, h) tile list) and number of tiles
   int r0;          // full: resident-list offset of sequence b
+  int nres;        // full: resident chunks of sequence b
   int lo, span;    // ring: first attended position of the block and the union span length
   int s_lo;        // ring: slot of position lo
   bool bad;        // the sequence's q or L is out of range: it is skipped
 };
 
-template <bool RING>
+template <bool RING, int CPT>
 __device__ __forceinline__ Work make_work(const AttnParams& p) {
   Work w;
   w.b = blockIdx.z;
@@ -112,6 +133,7 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
   w.tb = 0;
   w.nt = 0;
   w.r0 = 0;
+  w.nres = 0;
   w.lo = 0;
   w.span = 0;
   w.s_lo = 0;
@@ -125,8 +147,8 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
   int n_tiles;
   if (!RING) {
     w.r0 = p.cu_res[w.b];
-    n_tiles = p.cu_res[w.b + 1] - w.r0;
-    if (n_tiles < 0) n_tiles = 0;
+    w.nres = max(0, p.cu_res[w.b + 1] - w.r0);
+    n_tiles = (w.nres + CPT - 1) / CPT;
   } else {
     const int R = p.ring_len;
     int phi = p.ring_off[w.b];
@@ -142,21 +164,26 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
   return w;
 }
 
-// Tile geometry: the TMA row coordinate of the tile's first token, and what the mask needs.
+// Geometry of chunk c of tile j: the TMA row coordinate of its first token, and what the mask
+// needs.
 struct Tile {
   int y;          // row of the 2-D [rows][d] view of the pool / ring
   int base;       // full: position of token 0; ring: offset (from s_lo, mod R) of slot 0
   bool valid;     // full: slot and chunk id in range
+  bool present;   // full: the sequence has this chunk (the last tile may hold one chunk only)
 };
 
-template <bool RING>
-__device__ __forceinline__ Tile tile_at(const AttnParams& p, const Work& w, int j) {
+template <bool RING, int CPT>
+__device__ __forceinline__ Tile tile_at(const AttnParams& p, const Work& w, int j, int c) {
   Tile t;
+  t.present = true;
   if (!RING) {
-    const int idx = w.r0 + w.tb + j;
-    const int cid = p.res_ids[idx];
-    const int slot = p.res_slots[idx];
-    t.valid = cid >= 0 && cid < (1 << 25) && slot >= 0 && slot < p.num_slots;
+    const int e = (w.tb + j) * CPT + c;
+    t.present = e < w.nres;
+    const int idx = w.r0 + (t.present ? e : 0);
+    const int cid = t.present ? p.res_ids[idx] : -1;
+    const int slot = t.present ? p.res_slots[idx] : -1;
+    t.valid = t.present && cid >= 0 && cid < (1 << 25) && slot >= 0 && slot < p.num_slots;
     t.y = (t.valid ? (slot * p.hkv + w.h) : w.h) * kChunk;
     t.base = t.valid ? cid * kChunk : 0;
   } else {
@@ -184,6 +211,16 @@ __device__ __forceinline__ bool key_in_union(const AttnParams& p, const Work& w,
     *pos_out = w.lo + off;
     return off < w.span;
   }
+}
+
+// Does some key of the tile lie outside the union span (so that its V row must be zeroed)? Full:
+// the tile's chunk is invalid or its last key is at or past L. Ring: offsets run base, base + 1, ...
+// (mod R); a tile that wraps holds offsets near R, past the span (the ring holds at least the span
+// plus one tile), so the tile is clean only when base + 63 < span.
+template <bool RING>
+__device__ __forceinline__ bool tile_has_outside_keys(const Work& w, const Tile& t) {
+  if (!RING) return !t.valid || t.base + kChunk - 1 >= w.L;
+  return t.base + kChunk - 1 >= w.span;
 }
 
 // The keys of a tile that one row attends form an interval [klo, khi] of tile indices:
@@ -217,16 +254,16 @@ __device__ __forceinline__ uint32_t staged_offset(int r, int col) {
   return static_cast<uint32_t>((r * HD + ((c ^ ((r >> 2) & 7)) << 2) + (col & 3)) * 4);
 }
 
-template <int HD, bool RING, bool MERGE>
+template <int HD, bool RING, bool MERGE, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
-  using C = Cfg<HD, MERGE>;
+  using C = Cfg<HD, RING, MERGE, WIDE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::kQBytes;
-  uint8_t* sV = sK + C::kStages * C::kTileBytes;
+  uint8_t* sV = sK + C::kKStages * C::kTileBytes;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOffset);
 
   const int warp = threadIdx.x >> 5;
@@ -234,12 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- prologue (overlaps the previous kernel under programmatic dependent launch) ----------
   if (threadIdx.x == kProducerWarp * 32) {
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
     }
-    for (int i = 0; i < kSBufs; ++i) {
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int i = 0; i < kGeo; ++i) mbar_init(&bars->geo_full[i], 1);
+    for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i][0], kSoftmaxThreads / 2);
       mbar_init(&bars->p_full[i][1], kSoftmaxThreads / 2);
@@ -268,155 +309,175 @@ __global__ void __launch_bounds__(kThreads, 1)
   // griddepcontrol.wait still waits for this grid to complete.
   pdl_launch_dependents();
   pdl_wait();
-  const Work w = make_work<RING>(p);
+  const Work w = make_work<RING, C::kCPT>(p);
   if (w.bad && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, kErrDeviceInput);
 
-  const uint32_t idesc_s = idesc_bf16_f32(128, kChunk, 0, 0);
+  const uint32_t idesc_s = idesc_bf16_f32(128, C::kKT, 0, 0);
   const uint32_t idesc_pv = idesc_bf16_f32(128, HD, 0, 1);
   const size_t pidx = (static_cast<size_t>(w.b) * p.hkv + w.h) * p.num_splits + w.s;
 
   if (warp == kProducerWarp) {
-    // ------------------------------ TMA producer -----------------------------------------
+    // ------------------------------ K producer (and tile geometry) -----------------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       auto prefetch_tile = [&](int f) {
-        const Tile tf = tile_at<RING>(p, w, f);
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_prefetch_2d(&tmap_k, bx * 64, tf.y);
-          tma_prefetch_2d(&tmap_v, bx * 64, tf.y);
+        for (int c = 0; c < C::kCPT; ++c) {
+          const Tile tf = tile_at<RING, C::kCPT>(p, w, f, c);
+          if (!tf.present) continue;
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            tma_prefetch_2d(&tmap_k, bx * 64, tf.y);
+            tma_prefetch_2d(&tmap_v, bx * 64, tf.y);
+          }
         }
       };
       int issued = 0;
       bool reported = false;
       for (int j = 0; j < w.nt; ++j) {
-        const int st = j % C::kStages;
-        if (j >= C::kStages && !mbar_wait(&bars->kv_empty[st], ((j / C::kStages) - 1) & 1, abort, p.err)) break;
-        const Tile t = tile_at<RING>(p, w, j);
-        if (!t.valid && !reported) {
-          atomicOr(p.err, kErrDeviceInput);
-          reported = true;
+        const int st = j % C::kKStages;
+        if (j >= C::kKStages && !mbar_wait(&bars->k_empty[st], ((j / C::kKStages) - 1) & 1, abort, p.err)) break;
+        Tile t[C::kCPT];
+        int n_present = 0;
+        bool zero = false;
+        const int g = j % kGeo;
+#pragma unroll
+        for (int c = 0; c < C::kCPT; ++c) {
+          t[c] = tile_at<RING, C::kCPT>(p, w, j, c);
+          if (t[c].present && !t[c].valid && !reported) {
+            atomicOr(p.err, kErrDeviceInput);
+            reported = true;
+          }
+          bars->tile_base[g][c] = t[c].base;
+          bars->tile_valid[g][c] = t[c].valid ? 1 : 0;
+          zero = zero || !t[c].present || tile_has_outside_keys<RING>(w, t[c]);
+          n_present += t[c].present ? 1 : 0;
         }
-        bars->tile_base[st] = t.base;
-        bars->tile_valid[st] = t.valid ? 1 : 0;
-        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+        bars->tile_zero[g] = zero ? 1 : 0;
+        mbar_arrive(&bars->geo_full[g]);
+        // A chunk the sequence lacks is not loaded: its K and V rows keep stale data, which the
+        // mask and the V zeroing make harmless.
+        mbar_arrive_expect_tx(&bars->k_full[st], n_present * C::kChunkBytes);
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &tmap_k, &bars->k_full[st], bx * 64, t.y, pol);
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
+        for (int c = 0; c < C::kCPT; ++c) {
+          if (!t[c].present) continue;
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &tmap_v, &bars->v_full[st], bx * 64, t.y, pol);
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes + c * C::kChunkRowsBytes, &tmap_k,
+                        &bars->k_full[st], bx * 64, t[c].y, pol);
+        }
         // Ask L2 for the tiles that follow the shared-memory stages, so that more of the stream is
         // in flight from HBM than the stages alone can hold.
-        if (j == C::kStages - 1) {
-          for (int f = C::kStages; f < C::kStages + kPrefetch && f < w.nt; ++f) prefetch_tile(f);
-        } else if (j >= C::kStages && j + kPrefetch < w.nt) {
+        if (j == C::kKStages - 1) {
+          for (int f = C::kKStages; f < C::kKStages + kPrefetch && f < w.nt; ++f) prefetch_tile(f);
+        } else if (j >= C::kKStages && j + kPrefetch < w.nt) {
           prefetch_tile(j + kPrefetch);
         }
         issued = j + 1;
       }
       if (*abort) {
         // Let every copy still in flight land before the CTA can exit.
-        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
-          mbar_drain(&bars->k_full[j % C::kStages], (j / C::kStages) & 1);
-          mbar_drain(&bars->v_full[j % C::kStages], (j / C::kStages) & 1);
+        for (int j = max(0, issued - C::kKStages); j < issued; ++j)
+          mbar_drain(&bars->k_full[j % C::kKStages], (j / C::kKStages) & 1);
+      }
+    }
+  } else if (warp == kVProducerWarp) {
+    // ------------------------------ V producer --------------------------------------------
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int issued = 0;
+      for (int j = 0; j < w.nt; ++j) {
+        const int st = j % C::kVStages;
+        if (j >= C::kVStages && !mbar_wait(&bars->v_empty[st], ((j / C::kVStages) - 1) & 1, abort, p.err)) break;
+        Tile t[C::kCPT];
+        int n_present = 0;
+#pragma unroll
+        for (int c = 0; c < C::kCPT; ++c) {
+          t[c] = tile_at<RING, C::kCPT>(p, w, j, c);
+          n_present += t[c].present ? 1 : 0;
         }
+        mbar_arrive_expect_tx(&bars->v_full[st], n_present * C::kChunkBytes);
+#pragma unroll
+        for (int c = 0; c < C::kCPT; ++c) {
+          if (!t[c].present) continue;
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes + c * C::kChunkRowsBytes, &tmap_v,
+                        &bars->v_full[st], bx * 64, t[c].y, pol);
+        }
+        issued = j + 1;
+      }
+      if (*abort) {
+        for (int j = max(0, issued - C::kVStages); j < issued; ++j)
+          mbar_drain(&bars->v_full[j % C::kVStages], (j / C::kVStages) & 1);
       }
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------ MMA issuer -------------------------------------------
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_ready, 0, abort, p.err));
-    tc_fence_after();
-    const uint32_t qaddr = smem_u32(sQ);
-    // S_j = Q K_j^T into S buffer j % 3. Before P.V of tile jp, S of tiles up to jp is issued
-    // (waiting for their K if need be: the softmax of tile jp needs S_jp), and S of tiles up to
-    // jp + 2 only if their K has already landed, so that P.V never waits for a later tile's K and
-    // each stage is released as soon as its P.V completes. S_{jp+2} goes into the buffer that P.V
-    // of tile jp-1, issued before it, reads P from: MMAs run in issue order.
-    int next_s = 0;
-    auto issue_s = [&](int j) {
-      const int st = j % C::kStages;
+    // ------------------------------ MMA issuer (one lane) ---------------------------------
+    // tcgen05.mma issue blocks while the tensor pipe is busy, so the tensor core idles whenever
+    // this thread does anything else: it only waits on barriers and issues.
+    if (lane == 0) {
+      bool ok = mbar_wait(&bars->q_ready, 0, abort, p.err);
       tc_fence_after();
-      if (lane == 0) {
+      const uint32_t qaddr = smem_u32(sQ);
+      // S_j = Q K_j^T into S buffer j % B (B = kSBufs). Before P.V of tile jp, S of tiles up to jp
+      // is issued (waiting for their K if need be: the softmax of tile jp needs S_jp), and S of
+      // tiles up to jp + B - 1 only if their K has already landed, so that P.V never waits for a
+      // later tile's K and each stage is released as soon as its P.V completes. S_{jp+B-1} goes
+      // into the buffer that P.V of tile jp-1, issued before it, reads P from: MMAs run in issue
+      // order.
+      int next_s = 0;
+      auto issue_s = [&](int j) {
+        const int st = j % C::kKStages;
+        tc_fence_after();
         const uint32_t kaddr = smem_u32(sK + st * C::kTileBytes);
-        const uint32_t d_s = tbase + kColS + (j % kSBufs) * 64;
+        const uint32_t d_s = tbase + kColS + (j % C::kSBufs) * C::kKT;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint64_t a = sw128_desc(qaddr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bdesc = sw128_desc(kaddr + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
           mma_ss(d_s, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->s_full[j % kSBufs]);
-      }
-      __syncwarp();
-    };
-    for (int jp = 0; ok && jp < w.nt; ++jp) {
-      while (ok && next_s <= jp) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[next_s % C::kStages], (next_s / C::kStages) & 1,
-                                               abort, p.err));
-        if (ok) issue_s(next_s++);
-      }
-      while (ok && next_s < w.nt && next_s <= jp + 2 &&
-             __all_sync(0xffffffffu, mbar_test_wait(&bars->k_full[next_s % C::kStages], (next_s / C::kStages) & 1)))
-        issue_s(next_s++);
-      if (!ok) break;
-      // O_h += P_h V_h for tile jp, h = 0 (keys 0..31) and 1 (keys 32..63)
-      const int st = jp % C::kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (jp / C::kStages) & 1, abort, p.err));
-      if (!ok) break;
-      // Keys outside every query's range may hold anything (stale ring slots, the unused tail of
-      // the last chunk). P is 0 there, but 0 * NaN is NaN on the tensor core, so their V rows are
-      // zeroed before the MMA reads them.
-      {
-        Tile t;
-        t.base = bars->tile_base[st];
-        t.valid = bars->tile_valid[st] != 0;
-        uint8_t* vt = sV + st * C::kTileBytes;
-        bool any = false;
-        for (int k = lane; k < kChunk; k += 32) {
-          int pos;
-          if (!key_in_union<RING>(p, w, t, k, &pos)) {
-            any = true;
-#pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx) {
-              uint4* row = reinterpret_cast<uint4*>(vt + bx * C::kBoxBytes + k * 128);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
+        mma_commit(&bars->s_full[j % C::kSBufs]);
+        mma_commit(&bars->k_empty[st]);                 // S_j has read K_j
+      };
+      for (int jp = 0; ok && jp < w.nt; ++jp) {
+        while (ok && next_s <= jp) {
+          ok = mbar_wait(&bars->k_full[next_s % C::kKStages], (next_s / C::kKStages) & 1, abort, p.err);
+          if (ok) issue_s(next_s++);
         }
-        if (any) fence_proxy_async_smem();
-        __syncwarp();
-      }
-      const uint32_t vaddr = smem_u32(sV + st * C::kTileBytes);
-      const int sb = jp % kSBufs;
-      for (int h = 0; h < 2; ++h) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_full[sb][h], (jp / kSBufs) & 1, abort, p.err));
+        while (ok && next_s < w.nt && next_s <= jp + C::kSBufs - 1 &&
+               mbar_test_wait(&bars->k_full[next_s % C::kKStages], (next_s / C::kKStages) & 1))
+          issue_s(next_s++);
         if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
+        // O_h += P_h V_h for tile jp over the keys [h kKH, (h + 1) kKH) of warpgroup h, which has
+        // zeroed the V rows of its keys that lie outside every query's range before arriving.
+        const int st = jp % C::kVStages;
+        ok = mbar_wait(&bars->v_full[st], (jp / C::kVStages) & 1, abort, p.err);
+        if (!ok) break;
+        const uint32_t vaddr = smem_u32(sV + st * C::kTileBytes);
+        const int sb = jp % C::kSBufs;
+        for (int h = 0; h < 2; ++h) {
+          ok = mbar_wait(&bars->p_full[sb][h], (jp / C::kSBufs) & 1, abort, p.err);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t bdesc = sw128_desc(vaddr + (2 * h + kk) * 2048, C::kBoxBytes, 1024);
-            mma_ts(tbase + kColO + h * 128, tbase + kColS + sb * 64 + h * 32 + kk * 8, bdesc, idesc_pv,
+          for (int kk = 0; kk < C::kKH / 16; ++kk) {
+            const uint64_t bdesc = sw128_desc(vaddr + (h * C::kKH + 16 * kk) * 128, C::kBoxBytes, 1024);
+            mma_ts(tbase + kColO + h * 128, tbase + kColS + sb * C::kKT + h * C::kKH + kk * 8, bdesc, idesc_pv,
                    (jp > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->o_full[h][jp & 1]);
         }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) {
-        mma_commit(&bars->kv_empty[st]);
+        if (!ok) break;
+        mma_commit(&bars->v_empty[st]);
         if (jp == w.nt - 1) mma_commit(&bars->o_done);
       }
-      __syncwarp();
+      // Every MMA issued above completes before TMEM is freed.
+      mma_commit(&bars->drain);
+      mbar_drain(&bars->drain, 0);
     }
-    // Every MMA issued above completes before TMEM is freed.
-    if (lane == 0) mma_commit(&bars->drain);
     __syncwarp();
-    mbar_drain(&bars->drain, 0);
   } else {
     // ------------------------------ softmax / epilogue (warps 0-7) ------------------------
     const int wg = warp >> 2;                          // warpgroup: which 32 keys of a tile
@@ -446,42 +507,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int p_i = w.L - w.nq + qi;                   // this row's query position
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int k0 = wg * 32;                            // this warpgroup's first key in a tile
+    constexpr int KH = C::kKH;                         // keys of a tile this warpgroup takes
+    const int cw = C::kCPT == 2 ? wg : 0;              // the chunk that holds them
+    const int kofs = C::kCPT == 2 ? 0 : wg * KH;       // and the first one's index in that chunk
+    const uint32_t col_s = kColS + wg * KH;            // their S columns within a buffer
     const uint32_t col_o = kColO + wg * 128;           // this warpgroup's O accumulator
     float m_ref = -INFINITY;                           // this half's reference maximum
     float l_half = 0.f;                                // this half's row sum
     bool ok = true;
     for (int j = 0; j < w.nt; ++j) {
-      const int sb = j % kSBufs;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / kSBufs) & 1, abort, p.err));
+      const int sb = j % C::kSBufs;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[32];
-      tmem_ld32(lane_base + kColS + sb * 64 + k0, sr);
-      // The tile's geometry comes from the producer through shared memory (k_full has completed,
-      // since S_j has: this wait only makes the producer's writes visible).
-      const int st = j % C::kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (j / C::kStages) & 1, abort, p.err));
+      float sv[KH];
+      {
+        uint32_t sr[KH];
+        if constexpr (KH == 32)
+          tmem_ld32(lane_base + col_s + sb * C::kKT, sr);
+        else
+          tmem_ld64(lane_base + col_s + sb * C::kKT, sr);
+#pragma unroll
+        for (int k = 0; k < KH; ++k) sv[k] = __uint_as_float(sr[k]);
+      }
+      // The tile's geometry comes from the K producer through its ring. The entry is rewritten
+      // for tile j + kGeo only after S_{j + kGeo - kKStages} has read its K; that S needed its
+      // buffer back from P.V of tile j + kGeo - kKStages - kSBufs >= j, which waits for this
+      // warpgroup's P of that tile. So the entry is still this tile's, and its barrier is not a
+      // phase ahead.
+      const int g = j % kGeo;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[g], (j / kGeo) & 1, abort, p.err));
       if (!ok) break;
       Tile t;
-      t.base = bars->tile_base[st];
-      t.valid = bars->tile_valid[st] != 0;
+      t.base = bars->tile_base[g][cw];
+      t.valid = bars->tile_valid[g][cw] != 0;
       int klo = 0, khi = kChunk - 1;
       if (rv) key_interval<RING>(p, w, t, p_i, &klo, &khi);
-      klo -= k0;
-      khi -= k0;
+      klo -= kofs;
+      khi -= kofs;
       // Rows past the block (padding lanes) see Q = 0; their P and O rows are never read.
-      float sv[32];
-      if (__all_sync(0xffffffffu, klo <= 0 && khi >= 31)) {
+      if (!__all_sync(0xffffffffu, klo <= 0 && khi >= KH - 1)) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) sv[k] = __uint_as_float(sr[k]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) sv[k] = (k >= klo && k <= khi) ? __uint_as_float(sr[k]) : -INFINITY;
+        for (int k = 0; k < KH; ++k) sv[k] = (k >= klo && k <= khi) ? sv[k] : -INFINITY;
       }
       float mx[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(fmaxf(sv[u], sv[u + 8]), fmaxf(sv[u + 16], sv[u + 24]));
+      for (int u = 0; u < 8; ++u) mx[u] = sv[u];
+#pragma unroll
+      for (int k = 8; k < KH; ++k) mx[k & 7] = fmaxf(mx[k & 7], sv[k]);
       const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
       bool need_o = false;
@@ -494,10 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, need_o)) {
         // O_h holds the sum over tiles < j: wait for its P.V of tile j-1, then scale it. S_j was
-        // issued after P.V of tile j-3 (S_j needs the buffer it read) and has completed, so that
-        // P.V has too, and P.V of tile j+1 needs this tile's P: the
-        // barrier of odd or even tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after,
-        // so the parity wait for phase (j-1)/2 is exact.
+        // issued after P.V of tile j - kSBufs (S_j needs the buffer it read) and has completed, so
+        // that P.V has too, and P.V of tile j+1 needs this tile's P: the barrier of odd or even
+        // tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after, so the parity wait for
+        // phase (j-1)/2 is exact.
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err));
         if (!ok) break;
         tc_fence_after();
@@ -514,10 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // p = 2^(s * scale * log2e - m_ref); masked keys carry s = -inf and give exactly 0. A row that
       // has seen no key yet (m_ref = -inf) has only masked keys here, and uses 0 as reference.
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t pk[16];
+      uint32_t pk[KH / 2];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
+      for (int e = 0; e < KH / 2; ++e) {
         const float p0 = ex2_approx(fmaf(sv[2 * e], p.scale_log2, neg_m));
         const float p1 = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, neg_m));
         ps[e & 3] += p0 + p1;
@@ -525,8 +598,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       if (rv) l_half += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      tmem_st16(lane_base + kColS + sb * 64 + k0, pk);    // P_h over this half's own S columns
+      // P_h over the first half of this warpgroup's own S columns
+      if constexpr (KH == 32)
+        tmem_st16(lane_base + col_s + sb * C::kKT, pk);
+      else
+        tmem_st32(lane_base + col_s + sb * C::kKT, pk);
       tc_fence_before();
+      if (bars->tile_zero[g]) {
+        // Keys outside every query's range may hold anything (stale ring slots, the unused tail
+        // of the last chunk, a chunk the sequence lacks). P is 0 there, but 0 * NaN is NaN on the
+        // tensor core, so the V rows of this half's such keys are zeroed (whole 128-byte rows:
+        // the swizzle permutes 16-byte chunks within a row) before P.V reads them.
+        const int sv_st = j % C::kVStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[sv_st], (j / C::kVStages) & 1, abort, p.err));
+        if (!ok) break;
+        constexpr int kTPR = 128 / KH;                 // threads per key row
+        constexpr int kPerT = C::kBoxes * 8 / kTPR;    // 16-byte chunks each of them zeroes
+        const int tw = threadIdx.x & 127;
+        const int kz = tw / kTPR;
+        int pos;
+        if (!key_in_union<RING>(p, w, t, kofs + kz, &pos)) {
+          uint8_t* vt = sV + sv_st * C::kTileBytes;
+          const int row = wg * KH + kz;                // the key's row in the tile
+#pragma unroll
+          for (int c = (tw % kTPR) * kPerT; c < (tw % kTPR + 1) * kPerT; ++c)
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * C::kBoxBytes + row * 128 + (c & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+      }
       mbar_arrive(&bars->p_full[sb][wg]);
     }
     // ---- epilogue: merge the two halves into the split's partial (m, l, unnormalised O) ----
@@ -812,22 +912,23 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
 
 }  // namespace
 
-// Largest cluster of attend_kernel<HD, RING, true> CTAs that can be resident on the current
-// device (one CTA per SM: the cluster must fit in one GPC), cached per device.
+// Largest cluster of merging attend_kernel CTAs that can be resident on the current device (one
+// CTA per SM: the cluster must fit in one GPC), cached per device.
 template <int HD, bool RING>
 static int merge_cluster_limit() {
   static int limit[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (limit[dev] != 0) return limit[dev];
-  auto kern = attend_kernel<HD, RING, true>;
+  auto kern = attend_kernel<HD, RING, true, false>;
+  constexpr int kSmem = Cfg<HD, RING, true, false>::kSmemBytes;
   static size_t done[64] = {};
-  if (ensure_smem_limit(kern, Cfg<HD, true>::kSmemBytes, done) != cudaSuccess) return 0;
+  if (ensure_smem_limit(kern, kSmem, done) != cudaSuccess) return 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kMaxClusterSplits, 1, 1);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<HD, true>::kSmemBytes;
+  cfg.dynamicSmemBytes = kSmem;
   int n = 0;
   if (cudaOccupancyMaxPotentialClusterSize(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
@@ -837,12 +938,12 @@ static int merge_cluster_limit() {
   return limit[dev];
 }
 
-template <int HD, bool RING, bool MERGE>
+template <int HD, bool RING, bool MERGE, bool WIDE>
 static cudaError_t launch_attend_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                    int num_seqs, cudaStream_t stream) {
   static size_t done[64] = {};
-  auto kern = attend_kernel<HD, RING, MERGE>;
-  constexpr int kSmem = Cfg<HD, MERGE>::kSmemBytes;
+  auto kern = attend_kernel<HD, RING, MERGE, WIDE>;
+  constexpr int kSmem = Cfg<HD, RING, MERGE, WIDE>::kSmemBytes;
   cudaError_t e = ensure_smem_limit(kern, kSmem, done);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_splits, p.hkv, num_seqs);
@@ -859,20 +960,24 @@ int attend_merge_limit(bool ring, int head_dim) {
   return ring ? merge_cluster_limit<64, true>() : merge_cluster_limit<64, false>();
 }
 
-cudaError_t launch_attend(bool ring, int head_dim, bool merge, const AttnParams& p, const CUtensorMap& tk,
-                          const CUtensorMap& tv, int num_seqs, cudaStream_t stream) {
-  if (merge) {
-    if (head_dim == 128)
-      return ring ? launch_attend_t<128, true, true>(p, tk, tv, num_seqs, stream)
-                  : launch_attend_t<128, false, true>(p, tk, tv, num_seqs, stream);
-    return ring ? launch_attend_t<64, true, true>(p, tk, tv, num_seqs, stream)
-                : launch_attend_t<64, false, true>(p, tk, tv, num_seqs, stream);
+template <int HD>
+static cudaError_t launch_attend_hd(bool ring, AttnTiles tiles, const AttnParams& p, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, int num_seqs, cudaStream_t stream) {
+  if (ring)
+    return tiles == AttnTiles::kMerge ? launch_attend_t<HD, true, true, false>(p, tk, tv, num_seqs, stream)
+                                      : launch_attend_t<HD, true, false, false>(p, tk, tv, num_seqs, stream);
+  switch (tiles) {
+    case AttnTiles::kMerge: return launch_attend_t<HD, false, true, false>(p, tk, tv, num_seqs, stream);
+    case AttnTiles::kWide: return launch_attend_t<HD, false, false, true>(p, tk, tv, num_seqs, stream);
+    default: return launch_attend_t<HD, false, false, false>(p, tk, tv, num_seqs, stream);
   }
-  if (head_dim == 128)
-    return ring ? launch_attend_t<128, true, false>(p, tk, tv, num_seqs, stream)
-                : launch_attend_t<128, false, false>(p, tk, tv, num_seqs, stream);
-  return ring ? launch_attend_t<64, true, false>(p, tk, tv, num_seqs, stream)
-              : launch_attend_t<64, false, false>(p, tk, tv, num_seqs, stream);
+}
+
+cudaError_t launch_attend(bool ring, int head_dim, AttnTiles tiles, const AttnParams& p, const CUtensorMap& tk,
+                          const CUtensorMap& tv, int num_seqs, cudaStream_t stream) {
+  if (ring && tiles == AttnTiles::kWide) return cudaErrorInvalidValue;
+  if (head_dim == 128) return launch_attend_hd<128>(ring, tiles, p, tk, tv, num_seqs, stream);
+  return launch_attend_hd<64>(ring, tiles, p, tk, tv, num_seqs, stream);
 }
 
 cudaError_t launch_combine(int head_dim, const CombineParams& p, cudaStream_t stream) {

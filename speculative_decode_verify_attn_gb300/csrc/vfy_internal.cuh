@@ -63,11 +63,19 @@ struct CombineParams {
   int* err;
 };
 
-// merge_in_cluster: the grid's x dimension (the splits) is one cluster, which merges the splits
-// and writes p.out / p.lse itself (no combine launch follows). Returns cudaErrorNotSupported,
-// before launching anything, when such a cluster cannot be resident on this device.
-cudaError_t launch_attend(bool ring, int head_dim, bool merge_in_cluster, const AttnParams& p,
-                          const CUtensorMap& tk, const CUtensorMap& tv, int num_seqs, cudaStream_t stream);
+// How an attention launch tiles and finishes its work:
+//  kNarrow  one 64-token chunk per tile; the splits' partials go to the combine kernel
+//  kWide    two chunks per tile (full layers whose splits hold many chunks: fewer, larger steps
+//           for the same bytes); partials go to the combine kernel
+//  kMerge   one chunk per tile; the grid's x dimension (the splits) is one cluster, which merges
+//           the splits and writes p.out / p.lse itself (no combine launch follows). Returns
+//           cudaErrorNotSupported, before launching anything, when such a cluster cannot be
+//           resident on this device.
+enum class AttnTiles { kNarrow, kWide, kMerge };
+// A split of a full layer takes wide tiles from this many resident chunks on.
+constexpr int kWideMinChunks = 8;
+cudaError_t launch_attend(bool ring, int head_dim, AttnTiles tiles, const AttnParams& p, const CUtensorMap& tk,
+                          const CUtensorMap& tv, int num_seqs, cudaStream_t stream);
 cudaError_t launch_combine(int head_dim, const CombineParams& p, cudaStream_t stream);
 // The most splits one merging launch can take on the current device (0 on error).
 int attend_merge_limit(bool ring, int head_dim);

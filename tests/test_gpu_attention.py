@@ -188,6 +188,62 @@ def test_full_ragged_batch(H, vfy):
     assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
 
 
+# Splits over at least 8 resident chunks take tiles of two chunks. 150 chunks over 17 or 19 splits
+# give splits of 7 to 9 chunks, so some tiles hold one chunk only; 64 splits stay on 1-chunk tiles.
+@pytest.mark.parametrize("splits", [17, 19, 64])
+def test_full_wide_tiles(H, vfy, splits):
+    rng = np.random.default_rng(21)
+    ctx = make_ctx(vfy, synth.LAGUNA)
+    vfy.vfy_set_splits(ctx, splits, 0)
+    L = 150 * C - 37                                                      # ragged last chunk
+    qb, kp, vp, ids, slots = paged_case(rng, synth.LAGUNA, L, 17)
+    run_full_and_check(H, vfy, ctx, qb, kp, vp, ids, slots, L, f"wide splits={splits}")
+
+
+def test_full_wide_tiles_ragged_batch(H, vfy):
+    """Sequences of 150, 37 and 1 resident chunks with 17 splits: the long one takes two-chunk
+    tiles, and so does every sequence in the launch, down to one tile with a single chunk."""
+    rng = np.random.default_rng(22)
+    s = synth.LAGUNA
+    lens = [150 * C, 37 * C - 5, 50]
+    qs = [17, 9, 17]
+    cu_q = np.concatenate([[0], np.cumsum(qs)]).astype(np.int32)
+    n_per = [(L + C - 1) // C for L in lens]
+    total_slots = sum(n_per) + 3
+    perm = rng.permutation(total_slots)
+    kp = synth.normal_bf16(rng, (total_slots, s.num_kv_heads, C, s.head_dim))
+    vp = synth.normal_bf16(rng, (total_slots, s.num_kv_heads, C, s.head_dim))
+    qb = synth.normal_bf16(rng, (int(cu_q[-1]), s.num_q_heads, s.head_dim))
+    ids, slots, cu_res = [], [], [0]
+    off = 0
+    for n in n_per:
+        ids += list(range(n))
+        slots += perm[off:off + n].tolist()
+        off += n
+        cu_res.append(len(ids))
+    ids = np.array(ids, np.int32)
+    slots = np.array(slots, np.int32)
+    ctx = make_ctx(vfy, s, max_seqs=4)
+    vfy.vfy_set_splits(ctx, 17, 0)
+    got, lse = H.attend_full(ctx, qb, cu_q, kp, vp, ids, slots, cu_res, lens)
+    ref, rlse = O.attend_full(qb, cu_q, kp, vp, ids, slots, cu_res, lens)
+    assert_attn_close(got, ref, "wide ragged")
+    assert_lse_close(lse, rlse, "wide ragged")
+    assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
+
+
+def test_full_wide_tiles_bad_slot_is_reported(H, vfy):
+    rng = np.random.default_rng(23)
+    s = synth.LAGUNA
+    qb, kp, vp, ids, slots = paged_case(rng, s, 150 * C, 17)
+    slots = slots.copy()
+    slots[77] = 10_000_000
+    ctx = make_ctx(vfy, s)
+    vfy.vfy_set_splits(ctx, 17, 0)
+    H.attend_full(ctx, qb, [0, 17], kp, vp, ids, slots, [0, len(ids)], [150 * C])
+    assert vfy.vfy_get_status(ctx) == vfy.VFY_EDEVICE_INPUT
+
+
 def test_full_bad_slot_is_reported_not_faulted(H, vfy):
     rng = np.random.default_rng(7)
     s = synth.LAGUNA
