@@ -69,10 +69,10 @@ struct Cfg {
   static constexpr int kQBytes = kMaxRows * HD * 2;
   static constexpr int kTileBytes = kKT * HD * 2;
   static constexpr int kChunkBytes = kChunk * HD * 2;
-  // K and V stage rings. A K stage frees when S has read it, a V stage only after P.V, so the K
-  // ring runs further ahead.
-  static constexpr int kKStages = WIDE ? (HD == 128 ? 3 : 5) : (HD == 128 ? (MERGE ? 3 : 6) : 8);
-  static constexpr int kVStages = WIDE ? (HD == 128 ? 2 : 4) : (HD == 128 ? (MERGE ? 3 : 5) : 8);
+  // K and V stage rings. A K stage frees as soon as S has read it, a V stage only after P.V, a
+  // tile later; with wide tiles V gets the extra stage so that its loads start as far ahead.
+  static constexpr int kKStages = WIDE ? (HD == 128 ? 2 : 4) : (HD == 128 ? (MERGE ? 3 : 6) : 8);
+  static constexpr int kVStages = WIDE ? (HD == 128 ? 3 : 5) : (HD == 128 ? (MERGE ? 3 : 5) : 8);
   static_assert(kKStages <= 8 && kVStages <= 8 && kKStages + kSBufs <= kGeo, "rings");
   static_assert(kColS + kSBufs * kKT <= kTmemCols, "tensor memory");
   static constexpr int kRecvEntries = kMaxRows + kMaxClusterSplits;
