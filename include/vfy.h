@@ -75,7 +75,8 @@ typedef struct vfy_config {
   int ring_len;             /* ring slots per sequence and KV head (2048), multiple of 64 */
   int max_seqs;             /* largest num_seqs of any call */
   int max_queries_per_seq;  /* largest q = D + 1; q * G must be <= 128 */
-  int max_splits;           /* split-KV partitions per (sequence, KV head) the workspace holds */
+  int max_splits;           /* split-KV partitions per (sequence, KV head) the workspace holds,
+                               1..64 */
   float softmax_scale;      /* 0 -> 1 / sqrt(head_dim) */
 } vfy_config;
 
@@ -93,7 +94,15 @@ VFY_API vfy_status vfy_get_status(vfy_ctx* ctx, vfy_stream_t stream);
 /* A static string naming a status. */
 VFY_API const char* vfy_strerror(vfy_status status);
 
-/* Override the split counts chosen automatically (0 = automatic). Tuning knob. */
+/* Number of kernels the calls on this context have enqueued so far (a captured call counts once,
+ * however often its graph is replayed); 0 for NULL. Host-side bookkeeping, no device work. */
+VFY_API unsigned long long vfy_launch_count(const vfy_ctx* ctx);
+
+/* Override the split counts chosen automatically (0 = automatic; at most max_splits). Tuning
+ * knob; the results agree up to rounding for every split count. A layer whose splits per
+ * (sequence, KV head) fit one thread-block cluster (at most 16, and what one GPC holds) merges
+ * them inside its attention kernel; more splits go through a second, combine kernel. Full-layer
+ * splits over at least 8 resident chunks stream two chunks per pipeline step. */
 VFY_API vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits);
 
 /*

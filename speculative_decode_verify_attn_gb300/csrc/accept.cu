@@ -20,6 +20,7 @@ namespace vfy {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 8;     // float4 loads in flight per thread
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -57,15 +58,25 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
     const float* src = p.logits + static_cast<size_t>(row) * p.vocab;
     unsigned long long best = 0ull;
     if (VEC4) {
-      // v0 and the row start are multiples of 4 floats (16 bytes).
+      // v0 and the row start are multiples of 4 floats (16 bytes). All of a thread's loads of a
+      // round are issued before any is used, so the segment costs about one memory round trip.
       const float4* s4 = reinterpret_cast<const float4*>(src + v0);
       const int n4 = v1 > v0 ? (v1 - v0) >> 2 : 0;
-      for (int i = threadIdx.x; i < n4; i += kThreads) {
-        const float4 v = __ldcs(s4 + i);
-        const int base = v0 + 4 * i;
-        const unsigned long long k01 = umax64(pack(v.x, base), pack(v.y, base + 1));
-        const unsigned long long k23 = umax64(pack(v.z, base + 2), pack(v.w, base + 3));
-        best = umax64(best, umax64(k01, k23));
+      for (int i0 = threadIdx.x; i0 < n4; i0 += kThreads * kUnroll) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (i0 + u * kThreads < n4) v[u] = __ldcs(s4 + i0 + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = i0 + u * kThreads;
+          if (i < n4) {
+            const int base = v0 + 4 * i;
+            const unsigned long long k01 = umax64(pack(v[u].x, base), pack(v[u].y, base + 1));
+            const unsigned long long k23 = umax64(pack(v[u].z, base + 2), pack(v[u].w, base + 3));
+            best = umax64(best, umax64(k01, k23));
+          }
+        }
       }
       for (int i = v0 + 4 * n4 + threadIdx.x; i < v1; i += kThreads) best = umax64(best, pack(src[i], i));
     } else {

@@ -24,6 +24,7 @@ struct vfy_ctx {
   int* err;
   int full_splits;   // 0 = automatic
   int swa_splits;
+  unsigned long long launches;   // kernels enqueued through this context
 };
 
 namespace {
@@ -101,6 +102,8 @@ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
   } while (0)
 
 extern "C" {
+
+unsigned long long vfy_launch_count(const vfy_ctx* ctx) { return ctx != nullptr ? ctx->launches : 0ull; }
 
 const char* vfy_strerror(vfy_status s) {
   switch (s) {
@@ -239,6 +242,7 @@ vfy_status vfy_select_resident(vfy_ctx* ctx, const float* scores, const int32_t*
   p.pagein_count = pagein_count;
   p.err = ctx->err;
   VFY_CUDA(vfy::launch_select(p, reinterpret_cast<cudaStream_t>(stream)));
+  ++ctx->launches;
   return VFY_OK;
 }
 
@@ -283,6 +287,7 @@ vfy_status vfy_page_in(vfy_ctx* ctx, const uint16_t* host_k, const uint16_t* hos
   p.chunk_elems = static_cast<long long>(ctx->cfg.num_kv_heads) * kChunk * ctx->cfg.head_dim;
   p.err = ctx->err;
   VFY_CUDA(vfy::launch_page_in(p, s));
+  ++ctx->launches;
   return VFY_OK;
 }
 
@@ -349,6 +354,7 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   p.token_cap = num_seqs * c.max_queries_per_seq;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   VFY_CUDA(vfy::launch_attend(ring, c.head_dim, tiles, p, tk, tv, num_seqs, s));
+  ++ctx->launches;
   if (merge) return VFY_OK;
 
   vfy::CombineParams cp;
@@ -367,6 +373,7 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   cp.lse = lse;
   cp.err = ctx->err;
   VFY_CUDA(vfy::launch_combine(c.head_dim, cp, s));
+  ++ctx->launches;
   return VFY_OK;
 }
 
@@ -434,6 +441,7 @@ vfy_status vfy_accept(vfy_ctx* ctx, const float* logits, int vocab, const int32_
   p.err = ctx->err;
   const bool vec4 = (vocab % 4 == 0) && aligned16(logits);
   VFY_CUDA(vfy::launch_accept(p, vec4, reinterpret_cast<cudaStream_t>(stream)));
+  ++ctx->launches;
   return VFY_OK;
 }
 

@@ -21,10 +21,14 @@
 //              launches, which are latency-bound.
 //   warp 8     TMA producer of K tiles (a ring of smem stages, released when S has read them) and
 //              of the tile geometry the softmax needs (a ring of its own)
-//   warp 9     TMEM owner and MMA issuer (one lane)
-//   warp 10    TMA producer of V tiles (a ring released when P.V has read them)
-// Row r = i * G + g (query i, q-head g of the group) sits in TMEM lane (r % 4) * 32 + r / 4, so the
-// real rows spread over the four lane quarters and all four softmax warps share the work.
+//   warp 9     TMA producer of V tiles (a ring released when P.V has read them)
+//   warp 10    TMEM owner and MMA issuer (one lane)
+// Row r = i * G + g (query i, q-head g of the group) sits in TMEM lane r for r < 64, lane r + 32 for
+// 64 <= r < 96 and lane r - 32 above: lane quarter 2 holds rows only in blocks of more than 96.
+// Warps are spread over the SM's four sub-partitions by warp index mod 4, so the softmax warps of
+// quarter 2 (warps 2 and 6) then have nothing to compute, and the MMA issuer, warp 10, has its
+// sub-partition to itself: tcgen05.mma issue blocks while the tensor pipe is busy, so the
+// tensor core idles whenever that thread waits for an issue slot.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -38,8 +42,8 @@ namespace {
 constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kVProducerWarp = 10;
+constexpr int kVProducerWarp = 9;
+constexpr int kMmaWarp = 10;
 constexpr int kGeo = 16;          // tile-geometry ring: at least the K stages plus the S buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // two O accumulators (one per warpgroup) of d columns, 128 apart
@@ -419,7 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = mbar_wait(&bars->q_ready, 0, abort, p.err);
       tc_fence_after();
-      const uint32_t qaddr = smem_u32(sQ);
+      // Descriptors are built once: a descriptor's low 14 bits hold its address >> 4, and shared
+      // addresses stay below 256 KB, so adding a byte offset >> 4 moves it without carrying out of
+      // the field. The thread shares its sub-partition with two softmax warps, so every scalar
+      // instruction it saves shortens the time the tensor pipe waits for it.
+      const uint64_t qdesc = sw128_desc(smem_u32(sQ), 16, 1024);
+      const uint64_t kdesc = sw128_desc(smem_u32(sK), 16, 1024);
+      const uint64_t vdesc = sw128_desc(smem_u32(sV), C::kBoxBytes, 1024);
       // S_j = Q K_j^T into S buffer j % B (B = kSBufs). Before P.V of tile jp, S of tiles up to jp
       // is issued (waiting for their K if need be: the softmax of tile jp needs S_jp), and S of
       // tiles up to jp + B - 1 only if their K has already landed, so that P.V never waits for a
@@ -430,12 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_s = [&](int j) {
         const int st = j % C::kKStages;
         tc_fence_after();
-        const uint32_t kaddr = smem_u32(sK + st * C::kTileBytes);
+        const uint64_t kd = kdesc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
         const uint32_t d_s = tbase + kColS + (j % C::kSBufs) * C::kKT;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t a = sw128_desc(qaddr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bdesc = sw128_desc(kaddr + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t a = qdesc + static_cast<uint64_t>(((kk >> 2) * C::kQBoxBytes + (kk & 3) * 32) >> 4);
+          const uint64_t bdesc = kd + static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
           mma_ss(d_s, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full[j % C::kSBufs]);
@@ -455,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = jp % C::kVStages;
         ok = mbar_wait(&bars->v_full[st], (jp / C::kVStages) & 1, abort, p.err);
         if (!ok) break;
-        const uint32_t vaddr = smem_u32(sV + st * C::kTileBytes);
+        const uint64_t vd = vdesc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
         const int sb = jp % C::kSBufs;
         for (int h = 0; h < 2; ++h) {
           ok = mbar_wait(&bars->p_full[sb][h], (jp / C::kSBufs) & 1, abort, p.err);
@@ -463,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < C::kKH / 16; ++kk) {
-            const uint64_t bdesc = sw128_desc(vaddr + (h * C::kKH + 16 * kk) * 128, C::kBoxBytes, 1024);
+            const uint64_t bdesc = vd + static_cast<uint64_t>(((h * C::kKH + 16 * kk) * 128) >> 4);
             mma_ts(tbase + kColO + h * 128, tbase + kColS + sb * C::kKT + h * C::kKH + kk * 8, bdesc, idesc_pv,
                    (jp > 0 || kk > 0) ? 1u : 0u);
           }
@@ -483,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = warp >> 2;                          // warpgroup: which 32 keys of a tile
     const int quarter = warp & 3;                      // TMEM lane quarter
     const int mrow = quarter * 32 + lane;              // TMEM lane and Q smem row
-    const int r = lane * 4 + quarter;                  // block row held by this lane
+    const int r = lane + (quarter == 2 ? 96 : quarter == 3 ? 64 : quarter * 32);   // block row of this lane
+    const bool active = __any_sync(0xffffffffu, r < w.rows);   // the warp holds a row of the block
     const bool rv = r < w.rows;
     const int qi = rv ? r / p.group : 0;
     const int g = rv ? r % p.group : 0;
@@ -520,91 +531,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
-      float sv[KH];
-      {
-        uint32_t sr[KH];
-        if constexpr (KH == 32)
-          tmem_ld32(lane_base + col_s + sb * C::kKT, sr);
-        else
-          tmem_ld64(lane_base + col_s + sb * C::kKT, sr);
-#pragma unroll
-        for (int k = 0; k < KH; ++k) sv[k] = __uint_as_float(sr[k]);
-      }
       // The tile's geometry comes from the K producer through its ring. The entry is rewritten
       // for tile j + kGeo only after S_{j + kGeo - kKStages} has read its K; that S needed its
       // buffer back from P.V of tile j + kGeo - kKStages - kSBufs >= j, which waits for this
       // warpgroup's P of that tile. So the entry is still this tile's, and its barrier is not a
       // phase ahead.
-      const int g = j % kGeo;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[g], (j / kGeo) & 1, abort, p.err));
+      const int gs = j % kGeo;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[gs], (j / kGeo) & 1, abort, p.err));
       if (!ok) break;
       Tile t;
-      t.base = bars->tile_base[g][cw];
-      t.valid = bars->tile_valid[g][cw] != 0;
-      int klo = 0, khi = kChunk - 1;
-      if (rv) key_interval<RING>(p, w, t, p_i, &klo, &khi);
-      klo -= kofs;
-      khi -= kofs;
-      // Rows past the block (padding lanes) see Q = 0; their P and O rows are never read.
-      if (!__all_sync(0xffffffffu, klo <= 0 && khi >= KH - 1)) {
+      t.base = bars->tile_base[gs][cw];
+      t.valid = bars->tile_valid[gs][cw] != 0;
+      if (active) {
+        // (A warp without rows of the block only keeps the barrier protocol: its P and O lanes are
+        // never read.)
+        float sv[KH];
+        {
+          uint32_t sr[KH];
+          if constexpr (KH == 32)
+            tmem_ld32(lane_base + col_s + sb * C::kKT, sr);
+          else
+            tmem_ld64(lane_base + col_s + sb * C::kKT, sr);
 #pragma unroll
-        for (int k = 0; k < KH; ++k) sv[k] = (k >= klo && k <= khi) ? sv[k] : -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = sv[u];
-#pragma unroll
-      for (int k = 8; k < KH; ++k) mx[k & 7] = fmaxf(mx[k & 7], sv[k]);
-      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
-      bool need_o = false;
-      float alpha = 1.f;
-      if (m_tile > m_ref + kRescaleLog2) {
-        need_o = m_ref != -INFINITY;                  // O_h already holds weighted values
-        alpha = ex2_approx(m_ref - m_tile);           // 0 when m_ref = -inf
-        l_half *= alpha;
-        m_ref = m_tile;
-      }
-      if (__any_sync(0xffffffffu, need_o)) {
-        // O_h holds the sum over tiles < j: wait for its P.V of tile j-1, then scale it. S_j was
-        // issued after P.V of tile j - kSBufs (S_j needs the buffer it read) and has completed, so
-        // that P.V has too, and P.V of tile j+1 needs this tile's P: the barrier of odd or even
-        // tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after, so the parity wait for
-        // phase (j-1)/2 is exact.
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err));
-        if (!ok) break;
-        tc_fence_after();
-        const float a = need_o ? alpha : 1.f;
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + col_o + c * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-          tmem_st32(lane_base + col_o + c * 32, o);
+          for (int k = 0; k < KH; ++k) sv[k] = __uint_as_float(sr[k]);
         }
-      }
-      // p = 2^(s * scale * log2e - m_ref); masked keys carry s = -inf and give exactly 0. A row that
-      // has seen no key yet (m_ref = -inf) has only masked keys here, and uses 0 as reference.
-      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t pk[KH / 2];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        int klo = 0, khi = kChunk - 1;
+        if (rv) key_interval<RING>(p, w, t, p_i, &klo, &khi);
+        klo -= kofs;
+        khi -= kofs;
+        // Rows past the block (padding lanes) see Q = 0; their P and O rows are never read.
+        if (!__all_sync(0xffffffffu, klo <= 0 && khi >= KH - 1)) {
 #pragma unroll
-      for (int e = 0; e < KH / 2; ++e) {
-        const float p0 = ex2_approx(fmaf(sv[2 * e], p.scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, neg_m));
-        ps[e & 3] += p0 + p1;
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          for (int k = 0; k < KH; ++k) sv[k] = (k >= klo && k <= khi) ? sv[k] : -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = sv[u];
+#pragma unroll
+        for (int k = 8; k < KH; ++k) mx[k & 7] = fmaxf(mx[k & 7], sv[k]);
+        const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+        bool need_o = false;
+        float alpha = 1.f;
+        if (m_tile > m_ref + kRescaleLog2) {
+          need_o = m_ref != -INFINITY;                // O_h already holds weighted values
+          alpha = ex2_approx(m_ref - m_tile);         // 0 when m_ref = -inf
+          l_half *= alpha;
+          m_ref = m_tile;
+        }
+        if (__any_sync(0xffffffffu, need_o)) {
+          // O_h holds the sum over tiles < j: wait for its P.V of tile j-1, then scale it. S_j was
+          // issued after P.V of tile j - kSBufs (S_j needs the buffer it read) and has completed,
+          // so that P.V has too, and P.V of tile j+1 needs this tile's P: the barrier of odd or
+          // even tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after, so the parity
+          // wait for phase (j-1)/2 is exact.
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err));
+          if (!ok) break;
+          tc_fence_after();
+          const float a = need_o ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + col_o + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+            tmem_st32(lane_base + col_o + c * 32, o);
+          }
+        }
+        // p = 2^(s * scale * log2e - m_ref); masked keys carry s = -inf and give exactly 0. A row
+        // that has seen no key yet (m_ref = -inf) has only masked keys here, and uses 0 as
+        // reference.
+        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+        uint32_t pk[KH / 2];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < KH / 2; ++e) {
+          const float p0 = ex2_approx(fmaf(sv[2 * e], p.scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, neg_m));
+          ps[e & 3] += p0 + p1;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        if (rv) l_half += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        // P_h over the first half of this warpgroup's own S columns
+        if constexpr (KH == 32)
+          tmem_st16(lane_base + col_s + sb * C::kKT, pk);
+        else
+          tmem_st32(lane_base + col_s + sb * C::kKT, pk);
       }
-      if (rv) l_half += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      // P_h over the first half of this warpgroup's own S columns
-      if constexpr (KH == 32)
-        tmem_st16(lane_base + col_s + sb * C::kKT, pk);
-      else
-        tmem_st32(lane_base + col_s + sb * C::kKT, pk);
       tc_fence_before();
-      if (bars->tile_zero[g]) {
+      if (bars->tile_zero[gs]) {
         // Keys outside every query's range may hold anything (stale ring slots, the unused tail
         // of the last chunk, a chunk the sequence lacks). P is 0 there, but 0 * NaN is NaN on the
         // tensor core, so the V rows of this half's such keys are zeroed (whole 128-byte rows:

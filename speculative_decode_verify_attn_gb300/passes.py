@@ -148,6 +148,7 @@ class VerifyPass:
         # Paging gets the higher priority: its CTAs go ahead of queued layer CTAs as SMs free up.
         self.side = torch.cuda.Stream(device=dev, priority=-1)
         self.graph = None
+        self.kernels_per_pass = None
         self.step = 0
 
     # ------------------------------------------------------------------------------------------
@@ -164,8 +165,11 @@ class VerifyPass:
                          n_full * bytes_full + n_swa * bytes_swa + bytes_accept)
 
     def launches_per_step(self) -> int:
-        paging = 0 if self.all_resident else 1 + len(self.full_layers)
-        return paging + 2 * self.n_layers + 1
+        """Kernels one replay of the pass graph launches, as the library counted them while the
+        pass was captured (an attention call is one kernel or two, depending on its splits)."""
+        if self.kernels_per_pass is None:
+            raise RuntimeError("capture() the pass first")
+        return self.kernels_per_pass
 
     def set_step_scores(self, t: int):
         """Load step t's residency scores into the fixed score buffer (outside the graph)."""
@@ -249,9 +253,11 @@ class VerifyPass:
         self.graph = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
+        n0 = vfy.vfy_launch_count(self.ctx)
         with torch.cuda.stream(s):
             with torch.cuda.graph(self.graph, stream=s):
                 self.enqueue()
+        self.kernels_per_pass = vfy.vfy_launch_count(self.ctx) - n0
         torch.cuda.current_stream(self.dev).wait_stream(s)
         torch.cuda.synchronize(self.dev)
         self.step = 1

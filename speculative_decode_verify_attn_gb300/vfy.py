@@ -15,7 +15,7 @@ VFY_OK, VFY_EINVAL, VFY_ECUDA, VFY_ENOMEM, VFY_EUNSUPPORTED, VFY_EDEVICE_INPUT, 
 
 EXPORTS = ("vfy_create", "vfy_destroy", "vfy_get_status", "vfy_strerror", "vfy_set_splits",
            "vfy_select_resident", "vfy_page_in", "vfy_attend_full", "vfy_attend_swa", "vfy_accept",
-           "vfy_accept_static")
+           "vfy_accept_static", "vfy_launch_count")
 
 
 class VfyError(RuntimeError):
@@ -62,8 +62,10 @@ def lib() -> ctypes.CDLL:
         L.vfy_attend_swa.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]
         L.vfy_accept.argtypes = [_P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _P]
         L.vfy_accept_static.argtypes = [_P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P]
+        L.vfy_launch_count.argtypes = [_P]
+        L.vfy_launch_count.restype = ctypes.c_ulonglong
         for name in EXPORTS:
-            if name not in ("vfy_destroy", "vfy_strerror"):
+            if name not in ("vfy_destroy", "vfy_strerror", "vfy_launch_count"):
                 getattr(L, name).restype = _I
         _lib = L
     return _lib
@@ -157,6 +159,10 @@ def vfy_destroy(ctx: Context):
 
 def vfy_get_status(ctx: Context, stream=None) -> int:
     return lib().vfy_get_status(ctx.handle, _stream(stream))
+
+
+def vfy_launch_count(ctx: Context) -> int:
+    return int(lib().vfy_launch_count(ctx.handle))
 
 
 def vfy_set_splits(ctx: Context, full_splits: int = 0, swa_splits: int = 0):

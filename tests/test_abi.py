@@ -44,6 +44,10 @@ def test_only_the_abi_is_exported(lib):
     assert {s for s in text_syms if s.startswith("vfy_")} == set(declared_symbols())
 
 
+def test_launch_count_of_no_context_is_zero(lib):
+    assert lib.vfy_launch_count(None) == 0
+
+
 def test_strerror_needs_no_device(lib):
     from speculative_decode_verify_attn_gb300 import vfy
     assert vfy.strerror(vfy.VFY_OK) == "ok"

@@ -301,6 +301,20 @@ def test_swa_offsets_and_splits(H, vfy, phi, splits):
     assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
 
 
+@pytest.mark.parametrize("splits,kernels", [(10, 1), (16, 1), (17, 2)])
+def test_swa_kernels_per_call(H, vfy, splits, kernels):
+    """Splits that fit one cluster merge in the attention kernel; more add the combine kernel."""
+    rng = np.random.default_rng(31)
+    s = synth.LAGUNA
+    rk, rv = ring_case(rng, s, 1)
+    qb = synth.normal_bf16(rng, (17, s.num_q_heads, s.head_dim))
+    ctx = make_ctx(vfy, s)
+    vfy.vfy_set_splits(ctx, 0, splits)
+    n0 = vfy.vfy_launch_count(ctx)
+    H.attend_swa(ctx, qb, [0, 17], rk, rv, [5], [9000])
+    assert vfy.vfy_launch_count(ctx) - n0 == kernels
+
+
 @pytest.mark.parametrize("L", [1, 17, 100, 511, 512, 528, 529, 2000])
 def test_swa_short_sequences(H, vfy, L):
     rng = np.random.default_rng(100 + L)
