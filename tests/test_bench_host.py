@@ -72,3 +72,19 @@ def test_reference_arm_prints_its_line():
     assert line["metric"] == bench.METRIC
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu summary only while the kernel source is the
+    one the counters were taken on."""
+    src = tmp_path / "attend.cu"
+    src.write_bytes(b"kernel v1")
+    import hashlib
+    h = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    prof = tmp_path / "p.md"
+    prof.write_text(f"# x\n\ntraffic_bytes: 123\nsource_sha256_16: {h}\n")
+    monkeypatch.setattr(bench, "ATTEND_SRC", str(src))
+    monkeypatch.setattr(bench, "PROFILE_8K", str(prof))
+    assert bench.profiled_traffic() == 123
+    src.write_bytes(b"kernel v2")
+    assert bench.profiled_traffic() is None
