@@ -27,6 +27,16 @@ from . import synth, vfy
 CHUNK = 64
 
 
+def _packed(layout, dev):
+    """One uint8 device buffer with 256-byte-aligned byte views {name: view} for [(name, nbytes)]."""
+    offs, off = {}, 0
+    for name, nbytes in layout:
+        offs[name] = (off, nbytes)
+        off += (nbytes + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=dev)
+    return buf, {name: buf.narrow(0, o, n) for name, (o, n) in offs.items()}
+
+
 def is_full_layer(layer: int) -> bool:
     """3-in-4 pattern: layers 3, 7, 11, ... are full attention, the others window layers."""
     return layer % 4 == 3
@@ -90,7 +100,15 @@ class VerifyPass:
         self.rot = synth.rotating_residency(rng, self.n_chunks, self.k, workload.pagein_per_step or 16,
                                             self.L, self.q) if not all_resident else None
         self.cu_chunks = torch.tensor([0, self.n_chunks], dtype=torch.int32, device=dev)
-        self.scores = torch.zeros(self.n_chunks, dtype=torch.float32, device=dev)
+        # One device buffer holds every per-step input (block queries, residency scores, logits,
+        # drafts) and one holds every per-step result (accepted length, bonus, committed tokens),
+        # so a caller moves a step's data with one copy each way.
+        qbytes = self.n_layers * self.q * hq * d * 2
+        layout = [("q", qbytes), ("scores", self.n_chunks * 4), ("logits", self.q * workload.vocab * 4),
+                  ("drafts", max(self.q - 1, 1) * 4)]
+        self.inputs, views = _packed(layout, dev)
+        self.scores = views["scores"].view(torch.float32)
+        self.scores.zero_()
         self.slot_of_chunk = torch.full((self.n_chunks,), -1, dtype=torch.int32, device=dev)
         self.res_ids = torch.zeros(self.k, dtype=torch.int32, device=dev)
         self.res_slots = torch.zeros(self.k, dtype=torch.int32, device=dev)
@@ -130,7 +148,8 @@ class VerifyPass:
         self.cu_q = torch.tensor([0, self.q], dtype=torch.int32, device=dev)
         self.seq_len = torch.tensor([self.L], dtype=torch.int32, device=dev)
         # one buffer for all layers' block queries (one host->device copy per step end to end)
-        self.q_all = torch.randn((self.n_layers, self.q, hq, d), generator=gen, device=dev, dtype=torch.bfloat16)
+        self.q_all = views["q"].view(torch.bfloat16).view(self.n_layers, self.q, hq, d)
+        self.q_all.copy_(torch.randn((self.n_layers, self.q, hq, d), generator=gen, device=dev, dtype=torch.bfloat16))
         self.qs = [self.q_all[l] for l in range(self.n_layers)]
         self.out_all = torch.empty((self.n_layers, self.q, hq, d), device=dev, dtype=torch.bfloat16)
         self.outs = [self.out_all[l] for l in range(self.n_layers)]
@@ -139,12 +158,16 @@ class VerifyPass:
         # --- acceptance ---
         targets = rng.integers(0, self.vocab, self.q)
         self.targets = targets
-        self.logits = torch.from_numpy(synth.planted_logits(rng, targets, self.vocab)).to(dev)
-        self.drafts = torch.from_numpy(synth.drafts_matching(rng, targets, match_prob, self.vocab)).to(dev)
+        self.logits = views["logits"].view(torch.float32).view(self.q, self.vocab)
+        self.logits.copy_(torch.from_numpy(synth.planted_logits(rng, targets, self.vocab)))
+        drafts = torch.from_numpy(synth.drafts_matching(rng, targets, match_prob, self.vocab))
+        self.drafts = views["drafts"].view(torch.int32)[: drafts.numel()]
+        self.drafts.copy_(drafts)
         self.cu_rows = torch.tensor([0, self.q], dtype=torch.int32, device=dev)
-        self.accepted = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.bonus = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.committed = torch.zeros(self.q, dtype=torch.int32, device=dev)
+        self.results = torch.zeros(2 + self.q, dtype=torch.int32, device=dev)
+        self.accepted = self.results[0:1]
+        self.bonus = self.results[1:2]
+        self.committed = self.results[2:]
         # Paging gets the higher priority: its CTAs go ahead of queued layer CTAs as SMs free up.
         self.side = torch.cuda.Stream(device=dev, priority=-1)
         self.graph = None
