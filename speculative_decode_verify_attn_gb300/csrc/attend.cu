@@ -765,20 +765,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[kPer];
 #pragma unroll
       for (int x = 0; x < kPer; ++x) acc[x] = 0.f;
+      // No branch per split, so the loads of several splits can be in flight together. A split
+      // without data for the row sent no O row: its entry holds anything, and its zero weight
+      // selects it out.
+#pragma unroll 4
       for (int s = 0; s < n; ++s) {
         const float ws = __shfl_sync(0xffffffffu, wgt, s);
-        if (ws == 0.f) continue;                       // a split without data sent no O row
+        const bool use = ws != 0.f;
         const float* src = recv + static_cast<size_t>(k * n + s) * HD + lane * kPer;
         if constexpr (kPer == 4) {
           const float4 v = *reinterpret_cast<const float4*>(src);
-          acc[0] = fmaf(ws, v.x, acc[0]);
-          acc[1] = fmaf(ws, v.y, acc[1]);
-          acc[2] = fmaf(ws, v.z, acc[2]);
-          acc[3] = fmaf(ws, v.w, acc[3]);
+          acc[0] = use ? fmaf(ws, v.x, acc[0]) : acc[0];
+          acc[1] = use ? fmaf(ws, v.y, acc[1]) : acc[1];
+          acc[2] = use ? fmaf(ws, v.z, acc[2]) : acc[2];
+          acc[3] = use ? fmaf(ws, v.w, acc[3]) : acc[3];
         } else {
           const float2 v = *reinterpret_cast<const float2*>(src);
-          acc[0] = fmaf(ws, v.x, acc[0]);
-          acc[1] = fmaf(ws, v.y, acc[1]);
+          acc[0] = use ? fmaf(ws, v.x, acc[0]) : acc[0];
+          acc[1] = use ? fmaf(ws, v.y, acc[1]) : acc[1];
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
