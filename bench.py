@@ -304,6 +304,47 @@ def profiled_traffic():
         return None
 
 
+def drafter_ring_point(flush, local, rank, steps, peak):
+    """The drafter's context-KV ring: the 5 layers of the drafter head attend a 4096-position
+    window in an 8192-slot ring (16 proposals, 256K context, a wrapping write head), one graph.
+    Bytes per layer are the attended span's K and V: (4096 + 15) x 4 heads x 128 x 2 B x 2."""
+    import numpy as np
+    import torch
+
+    from speculative_decode_verify_attn_gb300 import synth, vfy
+    s = synth.LAGUNA
+    W, R, Q, NL = synth.DRAFTER_WINDOW, synth.DRAFTER_RING, synth.DRAFT, synth.DRAFTER_LAYERS
+    L = 262144
+    rng = np.random.default_rng(rank + 11)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(rank + 11)
+    ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, window=W, ring_len=R, max_seqs=1,
+                         max_queries_per_seq=Q, device=local)
+    shape = (1, s.num_kv_heads, R, s.head_dim)
+    kr = [torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16) for _ in range(NL)]
+    vr = [torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16) for _ in range(NL)]
+    q = torch.randn((NL, Q, s.num_q_heads, s.head_dim), generator=gen, device="cuda", dtype=torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty((NL, Q, s.num_q_heads), dtype=torch.float32, device="cuda")
+    i32 = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")
+    cu_q, seq_len = i32([0, Q]), i32([L])
+    phi = i32([synth.wrapping_ring_offset(rng, L, W + Q - 1, R)])
+
+    def layers():
+        for l in range(NL):
+            vfy.vfy_attend_swa(ctx, q[l], cu_q, kr[l], vr[l], phi, seq_len, out[l], lse[l], 1)
+
+    g = capture(layers)
+    mean_ms, _, _ = event_time_graph(g, flush, steps)
+    del g
+    ctx.close()
+    per_layer_bytes = (W + Q - 1) * s.num_kv_heads * s.head_dim * 2 * 2 + 2 * Q * s.num_q_heads * s.head_dim * 2
+    us = mean_ms * 1000
+    return {"layers": NL, "window": W, "ring": R, "us": round(us, 3), "us_per_layer": round(us / NL, 3),
+            "gbs": round(NL * per_layer_bytes / (mean_ms * 1e-3) / 1e9, 1),
+            "frac": round(NL * per_layer_bytes / (mean_ms * 1e-3) / 1e9 / peak, 4)}
+
+
 def capture(fn):
     import torch
     fn()                      # eager once (sets kernel attributes outside capture)
@@ -444,6 +485,7 @@ def run_ours(args):
                                              "frac": round(a_bytes / (a_mean * 1e-3) / 1e9 / peak, 4)}
         del g_ar
         ar.close()
+        extras["drafter_ring"] = drafter_ring_point(flush, local, rank, max(20, min(args.steps, 500)), peak)
 
     # end to end: inputs host->device from pinned memory, accepted tokens back, inside the timing
     e2e = None

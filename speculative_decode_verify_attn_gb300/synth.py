@@ -182,6 +182,13 @@ RING = 2048                       # ring slots
 DRAFT = 16                        # drafted tokens per step
 POOL_CHUNKS = 128                 # 8K-token resident pool = 128 chunks of 64
 VOCAB = 131072
+# The drafter's context-KV ring ('Laguna XS 2.1 33B on a RTX 3090', 'Three optimizations' item 2:
+# a feature window of up to 4K tokens, a position-indexed ring; 'The model ...': a 5-layer head
+# proposing 16 tokens). The pages give no drafter head counts: the target's 16 q / 4 KV x 128
+# are reused. The ring holds twice the window.
+DRAFTER_WINDOW = 4096
+DRAFTER_RING = 8192
+DRAFTER_LAYERS = 5
 
 
 @dataclass
