@@ -74,7 +74,9 @@ typedef struct vfy_config {
   int window;               /* sliding-window width in positions, self included (512) */
   int ring_len;             /* ring slots per sequence and KV head (2048), multiple of 64 */
   int max_seqs;             /* largest num_seqs of any call */
-  int max_queries_per_seq;  /* largest q = D + 1; q * G must be <= 128 */
+  int max_queries_per_seq;  /* largest q (D + 1 for a verify block; up to a prefill-sized block):
+                               q * G <= 4096. Each 128 of the q * G rows is one row tile,
+                               with CTAs and split partials of its own */
   int max_splits;           /* split-KV partitions per (sequence, KV head) the workspace holds,
                                1..64 */
   float softmax_scale;      /* 0 -> 1 / sqrt(head_dim) */

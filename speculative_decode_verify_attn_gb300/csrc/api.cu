@@ -1,4 +1,5 @@
 // Host side of the C ABI: context and workspace, argument validation, tensor maps, launches.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -25,6 +26,7 @@ struct vfy_ctx {
   int full_splits;   // 0 = automatic
   int swa_splits;
   unsigned long long launches;   // kernels enqueued through this context
+  int row_tiles;                 // ceil(max_queries_per_seq * G / 128)
 };
 
 namespace {
@@ -128,7 +130,7 @@ vfy_status vfy_create(const vfy_config* cfg_in, int device, vfy_ctx** out) {
   VFY_REQUIRE(cfg.max_seqs >= 1 && cfg.max_queries_per_seq >= 1 && cfg.max_splits >= 1);
   VFY_REQUIRE(cfg.max_splits <= 64 && cfg.max_seqs <= 65535 && cfg.num_kv_heads <= 65535);
   const int group = cfg.num_q_heads / cfg.num_kv_heads;
-  VFY_REQUIRE(static_cast<long long>(cfg.max_queries_per_seq) * group <= kMaxRows);
+  VFY_REQUIRE(static_cast<long long>(cfg.max_queries_per_seq) * group <= static_cast<long long>(kMaxRows) * vfy::kMaxRowTiles);
   VFY_REQUIRE(cfg.window >= 1 && cfg.ring_len >= kChunk && cfg.ring_len % kChunk == 0);
   // The ring must hold the union window of a block plus one tile of slack, so that the
   // slot-aligned tiles covering it are distinct.
@@ -154,7 +156,9 @@ vfy_status vfy_create(const vfy_config* cfg_in, int device, vfy_ctx** out) {
   ctx->num_sms = prop.multiProcessorCount;
   ctx->scale = cfg.softmax_scale > 0.f ? cfg.softmax_scale : 1.0f / std::sqrt(static_cast<float>(cfg.head_dim));
 
-  const size_t parts = static_cast<size_t>(cfg.max_seqs) * cfg.num_kv_heads * cfg.max_splits * kMaxRows;
+  ctx->row_tiles = ceil_div(static_cast<long long>(cfg.max_queries_per_seq) * group, kMaxRows);
+  const size_t parts =
+      static_cast<size_t>(cfg.max_seqs) * ctx->row_tiles * cfg.num_kv_heads * cfg.max_splits * kMaxRows;
   ctx->accept_rows_cap = cfg.max_seqs * cfg.max_queries_per_seq;
   bool ok = cudaMalloc(&ctx->part_o, parts * cfg.head_dim * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&ctx->part_ml, parts * 2 * sizeof(float)) == cudaSuccess &&
@@ -309,16 +313,17 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
     if (splits == 0) {
       // One wave of CTAs for one sequence; several waves for a batch, so that the hardware
       // scheduler can balance sequences of different lengths.
-      const int target = ctx->num_sms * (num_seqs > 1 ? 4 : 1);
-      splits = ceil_div(target, static_cast<long long>(hkv) * num_seqs);
+      const int target = ctx->num_sms * (num_seqs > 1 || ctx->row_tiles > 1 ? 4 : 1);
+      splits = ceil_div(target, static_cast<long long>(hkv) * num_seqs * ctx->row_tiles);
       splits = clampi(splits, 1, max_res > 0 ? max_res : 1);
     }
   } else {
     splits = ctx->swa_splits;
     if (splits == 0) {
-      const int max_tiles =
-          ceil_div(static_cast<long long>(kChunk - 1) + c.window + c.max_queries_per_seq - 1, kChunk);
-      splits = clampi(ceil_div(ctx->num_sms, static_cast<long long>(hkv) * num_seqs), 1, max_tiles);
+      // a row tile's queries: at most 128 / G of them
+      const int tile_q = std::min(c.max_queries_per_seq, ceil_div(kMaxRows, c.num_q_heads / hkv));
+      const int max_tiles = ceil_div(static_cast<long long>(kChunk - 1) + c.window + tile_q - 1, kChunk);
+      splits = clampi(ceil_div(ctx->num_sms, static_cast<long long>(hkv) * num_seqs * ctx->row_tiles), 1, max_tiles);
     }
   }
   splits = clampi(splits, 1, c.max_splits);
@@ -339,6 +344,7 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   p.group = c.num_q_heads / hkv;
   p.num_splits = splits;
   p.max_q = c.max_queries_per_seq;
+  p.row_tiles = ctx->row_tiles;
   p.scale_log2 = ctx->scale * 1.4426950408889634f;
   p.part_o = ctx->part_o;
   p.part_ml = ctx->part_ml;
@@ -366,6 +372,7 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   cp.group = p.group;
   cp.num_splits = splits;
   cp.max_q = c.max_queries_per_seq;
+  cp.row_tiles = ctx->row_tiles;
   cp.token_cap = num_seqs * c.max_queries_per_seq;
   cp.part_o = ctx->part_o;
   cp.part_ml = ctx->part_ml;

@@ -115,12 +115,14 @@ static_assert(sizeof(Bars) <= 4096, "barrier block overflows its reservation");
 // The per-CTA work item.
 struct Work {
   int b, h, s;
-  int q0, nq, rows;
+  int q0, nq;
+  int rt, row0;    // row tile: block rows [row0, row0 + rows) of the sequence's q * G
+  int rows;
   int L;
   int tb, nt;      // first tile (index within the (b, h) tile list) and number of tiles
   int r0;          // full: resident-list offset of sequence b
   int nres;        // full: resident chunks of sequence b
-  int lo, span;    // ring: first attended position of the block and the union span length
+  int lo, span;    // ring: first attended position of the tile's rows and the union span length
   int s_lo;        // ring: slot of position lo
   bool bad;        // the sequence's q or L is out of range: it is skipped
 };
@@ -128,7 +130,9 @@ struct Work {
 template <bool RING, int CPT>
 __device__ __forceinline__ Work make_work(const AttnParams& p) {
   Work w;
-  w.b = blockIdx.z;
+  w.b = static_cast<int>(blockIdx.z) / p.row_tiles;
+  w.rt = static_cast<int>(blockIdx.z) - w.b * p.row_tiles;
+  w.row0 = w.rt * kMaxRows;
   w.h = blockIdx.y;
   w.s = blockIdx.x;
   w.q0 = p.cu_q[w.b];
@@ -147,7 +151,8 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
     w.rows = 0;
     return w;
   }
-  w.rows = w.nq * p.group;
+  w.rows = min(kMaxRows, max(0, w.nq * p.group - w.row0));
+  if (w.rows == 0) return w;                     // a row tile past this sequence's block
   int n_tiles;
   if (!RING) {
     w.r0 = p.cu_res[w.b];
@@ -157,8 +162,11 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
     const int R = p.ring_len;
     int phi = p.ring_off[w.b];
     phi = ((phi % R) + R) % R;
-    w.lo = max(0, w.L - w.nq - p.window + 1);
-    w.span = w.L - w.lo;
+    // The tile's queries are i in [row0 / G, (row0 + rows - 1) / G], at positions L - nq + i.
+    const int i_first = w.row0 / p.group;
+    const int i_last = (w.row0 + w.rows - 1) / p.group;
+    w.lo = max(0, w.L - w.nq + i_first - p.window + 1);
+    w.span = w.L - w.nq + i_last + 1 - w.lo;
     w.s_lo = static_cast<int>((static_cast<long long>(w.lo) + phi) % R);
     n_tiles = w.span > 0 ? ((w.s_lo & (kChunk - 1)) + w.span + kChunk - 1) / kChunk : 0;
   }
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t idesc_s = idesc_bf16_f32(128, C::kKT, 0, 0);
   const uint32_t idesc_pv = idesc_bf16_f32(128, HD, 0, 1);
-  const size_t pidx = (static_cast<size_t>(w.b) * p.hkv + w.h) * p.num_splits + w.s;
+  const size_t pidx = ((static_cast<size_t>(w.b) * p.row_tiles + w.rt) * p.hkv + w.h) * p.num_splits + w.s;
 
   if (warp == kProducerWarp) {
     // ------------------------------ K producer (and tile geometry) -----------------------
@@ -493,9 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = warp >> 2;                          // warpgroup: which 32 keys of a tile
     const int quarter = warp & 3;                      // TMEM lane quarter
     const int mrow = quarter * 32 + lane;              // TMEM lane and Q smem row
-    const int r = lane + (quarter == 2 ? 96 : quarter == 3 ? 64 : quarter * 32);   // block row of this lane
-    const bool active = __any_sync(0xffffffffu, r < w.rows);   // the warp holds a row of the block
-    const bool rv = r < w.rows;
+    const int lr = lane + (quarter == 2 ? 96 : quarter == 3 ? 64 : quarter * 32);   // tile row of this lane
+    const bool active = __any_sync(0xffffffffu, lr < w.rows);  // the warp holds a row of the block
+    const bool rv = lr < w.rows;
+    const int r = w.row0 + lr;                         // block row: query r / G, q-head r % G
     const int qi = rv ? r / p.group : 0;
     const int g = rv ? r % p.group : 0;
     // Q row -> swizzled smem (the 128-byte swizzle TMA would apply: chunk c of row m at c ^ (m & 7)).
@@ -684,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rv && l_sum > 0.f) {
 #pragma unroll
             for (int x = 0; x < 32; x += 4)
-              *reinterpret_cast<float4*>(so + staged_offset<HD>(r, wg * (HD / 2) + c * 32 + x)) =
+              *reinterpret_cast<float4*>(so + staged_offset<HD>(lr, wg * (HD / 2) + c * 32 + x)) =
                   make_float4(w0 * __uint_as_float(o0[x]) + w1 * __uint_as_float(o1[x]),
                               w0 * __uint_as_float(o0[x + 1]) + w1 * __uint_as_float(o1[x + 1]),
                               w0 * __uint_as_float(o0[x + 2]) + w1 * __uint_as_float(o1[x + 2]),
@@ -692,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (wg == 0) bars->sml[r] = make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum);
+      if (wg == 0) bars->sml[lr] = make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum);
       named_bar_sync(1, kSoftmaxThreads);
       const int n = static_cast<int>(cluster_nctarank());
       const int rank = static_cast<int>(cluster_ctarank());
@@ -714,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (ok) {
       // warpgroup h writes columns [h d/2, (h + 1) d/2) of the merged O
-      float* dst = p.part_o + (pidx * kMaxRows + r) * HD + wg * (HD / 2);
+      float* dst = p.part_o + (pidx * kMaxRows + lr) * HD + wg * (HD / 2);
       if (w.nt > 0) {
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
@@ -733,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (rv && wg == 0) {
-        float2* ml = reinterpret_cast<float2*>(p.part_ml) + pidx * kMaxRows + r;
+        float2* ml = reinterpret_cast<float2*>(p.part_ml) + pidx * kMaxRows + lr;
         *ml = make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum);
       }
     }
@@ -786,8 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const int t = w.q0 + r / p.group;
-      const int hq = w.h * p.group + r % p.group;
+      const int t = w.q0 + (w.row0 + r) / p.group;      // r is the row within this tile
+      const int hq = w.h * p.group + (w.row0 + r) % p.group;
       if (t < p.token_cap) {
         uint16_t* dst = p.out + (static_cast<size_t>(t) * p.hq + hq) * HD + lane * kPer;
         if constexpr (kPer == 4) {
@@ -844,8 +853,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int nq = p.cu_q[b + 1] - p.cu_q[b];
   if (i < 0 || nq < 0 || nq > p.max_q || p.seq_len[b] < nq) return;   // skipped by the attention kernel too
   const int h = hq / p.group;
-  const int r = i * p.group + hq % p.group;
-  const size_t p0 = (static_cast<size_t>(b) * p.hkv + h) * p.num_splits;
+  const int rg = i * p.group + hq % p.group;              // block row
+  const int rt = rg / kMaxRows;                           // its row tile
+  const int r = rg - rt * kMaxRows;                       // and its row within the tile
+  const size_t p0 = ((static_cast<size_t>(b) * p.row_tiles + rt) * p.hkv + h) * p.num_splits;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
 
   // this warp's splits: s = warp + 4 u, u < nsub
@@ -967,7 +978,7 @@ static cudaError_t launch_attend_t(const AttnParams& p, const CUtensorMap& tk, c
   constexpr int kSmem = Cfg<HD, RING, MERGE, WIDE>::kSmemBytes;
   cudaError_t e = ensure_smem_limit(kern, kSmem, done);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.num_splits, p.hkv, num_seqs);
+  dim3 grid(p.num_splits, p.hkv, num_seqs * p.row_tiles);
   if constexpr (!MERGE) {
     return launch_pdl(kern, grid, dim3(kThreads), kSmem, stream, p, tk, tv);
   } else {

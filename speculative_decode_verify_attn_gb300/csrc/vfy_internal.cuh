@@ -11,7 +11,8 @@
 namespace vfy {
 
 constexpr int kChunk = 64;          // tokens per pool chunk and per attention tile
-constexpr int kMaxRows = 128;       // q * G rows of one (sequence, KV head) in the M = 128 MMA
+constexpr int kMaxRowTiles = 32;   // row tiles of 128 per (sequence, KV head): q * G <= 4096
+constexpr int kMaxRows = 128;       // block rows of one row tile: the M = 128 side of the MMA
 constexpr int kMaxSelectChunks = 32768;
 constexpr int kMaxSelectK = 4096;
 
@@ -33,6 +34,7 @@ struct AttnParams {
   int hq, hkv, group;
   int num_splits;
   int max_q;
+  int row_tiles;              // ceil(max_q * G / 128): grid z = B * row_tiles
   float scale_log2;           // softmax scale * log2(e)
   // split partials (workspace)
   float* part_o;              // [B][Hkv][splits][128][d]
@@ -55,6 +57,7 @@ struct CombineParams {
   int hq, hkv, group;
   int num_splits;
   int max_q;
+  int row_tiles;
   int token_cap;              // host bound on cu_q[B]
   const float* part_o;
   const float* part_ml;

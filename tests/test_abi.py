@@ -60,7 +60,7 @@ def test_create_validates_on_the_host(lib):
     cfg = vfy.Config(16, 4, 96, 64, 512, 2048, 1, 17, 64, 0.0)        # head_dim 96 unsupported
     h = ctypes.c_void_p()
     assert lib.vfy_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == vfy.VFY_EINVAL
-    cfg = vfy.Config(16, 4, 128, 64, 512, 2048, 1, 33, 64, 0.0)       # 33 queries x 4 > 128 rows
+    cfg = vfy.Config(16, 4, 128, 64, 512, 8192, 1, 1025, 64, 0.0)     # 1025 queries x 4 > 4096 rows
     assert lib.vfy_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == vfy.VFY_EINVAL
     cfg = vfy.Config(16, 4, 128, 32, 512, 2048, 1, 17, 64, 0.0)       # chunk must be 64
     assert lib.vfy_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == vfy.VFY_EINVAL
