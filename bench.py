@@ -154,6 +154,16 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor TFLOP/s: the measured burst figure, else the fallback (1.9 PFLOP/s)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 # ---------------------------------------------------------------------------------------------
 # CPU oracle sample (one host core)
 # ---------------------------------------------------------------------------------------------
@@ -302,6 +312,47 @@ def profiled_traffic():
         return int(fields["traffic_bytes"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def prefill_shaped_point(vp, flush, local, rank, steps, tf_peak):
+    """A 1024-query block (a prefill-sized batch through the pool) over one full layer of the
+    pass: the same 128 resident chunks at 256K context, the block at the end of the context.
+    Tensor-bound: useful flops = 4 per attended (row, key) pair and head dimension (S = Q K^T
+    and P V, 2 flops per multiply-add), counted exactly from the resident list."""
+    import numpy as np
+    import torch
+
+    from speculative_decode_verify_attn_gb300 import passes, synth, vfy
+    s = synth.LAGUNA
+    QB = 1024
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(rank + 21)
+    ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, max_seqs=1, max_queries_per_seq=QB,
+                         max_splits=16, device=local)
+    q = torch.randn((QB, s.num_q_heads, s.head_dim), generator=gen, device="cuda", dtype=torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty((QB, s.num_q_heads), dtype=torch.float32, device="cuda")
+    cu_q = torch.tensor([0, QB], dtype=torch.int32, device="cuda")
+    l = vp.full_layers[0]
+
+    def layer():
+        vfy.vfy_attend_full(ctx, q, cu_q, vp.pool_k[l], vp.pool_v[l], vp.k, vp.res_ids, vp.res_slots, vp.cu_res,
+                            vp.k, vp.seq_len, out, lse, 1)
+
+    g = capture(layer)
+    mean_ms, _, _ = event_time_graph(g, flush, steps)
+    del g
+    ctx.close()
+    ids = vp.res_ids.cpu().numpy().astype(np.int64)
+    L = vp.L
+    pos = (ids[:, None] * passes.CHUNK + np.arange(passes.CHUNK)[None, :]).ravel()
+    pos = np.sort(pos[pos < L])
+    p_i = L - QB + np.arange(QB)
+    pairs = int(np.searchsorted(pos, p_i, side="right").sum())     # attended (query, key) pairs
+    flops = pairs * s.num_q_heads * s.head_dim * 4
+    tf = flops / (mean_ms * 1e-3) / 1e12
+    return {"queries": QB, "resident_chunks": int(vp.k), "us": round(mean_ms * 1000, 2), "useful_gflop": round(flops / 1e9, 2),
+            "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / tf_peak, 4) if tf_peak else None}
 
 
 def drafter_ring_point(flush, local, rank, steps, peak):
@@ -486,6 +537,8 @@ def run_ours(args):
         del g_ar
         ar.close()
         extras["drafter_ring"] = drafter_ring_point(flush, local, rank, max(20, min(args.steps, 500)), peak)
+        extras["prefill_shaped_verify"] = prefill_shaped_point(vp, flush, local, rank, max(20, min(args.steps, 200)),
+                                                               bf16_peak())
 
     # end to end: inputs host->device from pinned memory, accepted tokens back, inside the timing
     e2e = None

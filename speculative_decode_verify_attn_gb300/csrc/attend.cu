@@ -130,7 +130,8 @@ struct Work {
 template <bool RING, int CPT>
 __device__ __forceinline__ Work make_work(const AttnParams& p) {
   Work w;
-  w.b = static_cast<int>(blockIdx.z) / p.row_tiles;
+  // A verify block is one row tile: no integer division on the path to the first load.
+  w.b = p.row_tiles == 1 ? static_cast<int>(blockIdx.z) : static_cast<int>(blockIdx.z) / p.row_tiles;
   w.rt = static_cast<int>(blockIdx.z) - w.b * p.row_tiles;
   w.row0 = w.rt * kMaxRows;
   w.h = blockIdx.y;
@@ -163,8 +164,9 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
     int phi = p.ring_off[w.b];
     phi = ((phi % R) + R) % R;
     // The tile's queries are i in [row0 / G, (row0 + rows - 1) / G], at positions L - nq + i.
-    const int i_first = w.row0 / p.group;
-    const int i_last = (w.row0 + w.rows - 1) / p.group;
+    const bool whole = p.row_tiles == 1;               // then the tile is the whole block
+    const int i_first = whole ? 0 : w.row0 / p.group;
+    const int i_last = whole ? w.nq - 1 : (w.row0 + w.rows - 1) / p.group;
     w.lo = max(0, w.L - w.nq + i_first - p.window + 1);
     w.span = w.L - w.nq + i_last + 1 - w.lo;
     w.s_lo = static_cast<int>((static_cast<long long>(w.lo) + phi) % R);
