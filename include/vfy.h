@@ -101,10 +101,11 @@ VFY_API const char* vfy_strerror(vfy_status status);
 VFY_API unsigned long long vfy_launch_count(const vfy_ctx* ctx);
 
 /* Override the split counts chosen automatically (0 = automatic; at most max_splits). Tuning
- * knob; the results agree up to rounding for every split count. A layer whose splits per
- * (sequence, KV head) fit one thread-block cluster (at most 16, and what one GPC holds) merges
- * them inside its attention kernel; more splits go through a second, combine kernel. Full-layer
- * splits over at least 8 resident chunks stream two chunks per pipeline step. */
+ * knob; the results agree up to rounding for every split count. Full-layer splits over at least
+ * 8 resident chunks stream two chunks per pipeline step and finish in a second, combine kernel.
+ * Otherwise a layer whose splits per (sequence, KV head) fit one thread-block cluster (at most
+ * 16, and what one GPC holds) merges them inside its attention kernel; more splits also go
+ * through the combine kernel. */
 VFY_API vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits);
 
 /*

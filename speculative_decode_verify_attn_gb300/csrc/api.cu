@@ -349,11 +349,12 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   p.part_o = ctx->part_o;
   p.part_ml = ctx->part_ml;
   p.err = ctx->err;
-  // Up to kMaxClusterSplits splits (and no more than one GPC holds) merge inside the attention
-  // kernel, as one thread-block cluster per (sequence, KV head); more go through the combine.
-  // Full-layer splits over many resident chunks take wide tiles.
-  const bool merge = splits <= vfy::kMaxClusterSplits && splits <= vfy::attend_merge_limit(ring, c.head_dim);
-  const bool wide = !ring && !merge && ceil_div(max_res, splits) >= vfy::kWideMinChunks;
+  // Full-layer splits over many resident chunks take wide tiles (their combine is a small part
+  // of a long split). Otherwise up to kMaxClusterSplits splits (and no more than one GPC holds)
+  // merge inside the attention kernel, as one thread-block cluster per (sequence, KV head, row
+  // tile); more go through the combine.
+  const bool wide = !ring && ceil_div(max_res > 0 ? max_res : 1, splits) >= vfy::kWideMinChunks;
+  const bool merge = !wide && splits <= vfy::kMaxClusterSplits && splits <= vfy::attend_merge_limit(ring, c.head_dim);
   const vfy::AttnTiles tiles = merge ? vfy::AttnTiles::kMerge : (wide ? vfy::AttnTiles::kWide : vfy::AttnTiles::kNarrow);
   p.out = merge ? out : nullptr;
   p.lse = merge ? lse : nullptr;

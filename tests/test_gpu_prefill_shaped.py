@@ -2,9 +2,9 @@
 ('Laguna XS 2.1 33B on a RTX 3090', 'Three optimizations' item 1: the prefill runs through the
 pool in 1024-token batches with CUDA-graph replay). Query i of a q-token block sits at position
 L - q + i and attends causally, so the block's q * G rows split into row tiles of 128, each with
-CTAs of its own. Checked against the fp64 oracle on every row: the full layer for automatic
-splits (two-chunk tiles and the combine), many splits (one-chunk tiles) and few splits (the
-cluster merge); the window layer; a ragged batch."""
+CTAs of its own. Checked against the fp64 oracle on every row: the full layer for automatic and
+few splits (two-chunk tiles and the combine), many splits (one-chunk tiles and the combine) and
+16 splits (4 chunks each: the cluster merge); the window layer; a ragged batch."""
 import numpy as np
 import pytest
 
@@ -39,7 +39,7 @@ def ctx_for(vfy, max_seqs=1, max_splits=48):
                           max_splits=max_splits, device=0)
 
 
-@pytest.mark.parametrize("splits", [0, 40, 3])
+@pytest.mark.parametrize("splits", [0, 40, 3, 16])
 def test_prefill_shaped_full_layer(H, vfy, splits):
     rng = np.random.default_rng(60 + splits)
     s = synth.LAGUNA
