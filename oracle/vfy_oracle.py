@@ -185,6 +185,54 @@ def page_in(host_k, host_v, k_pool, v_pool, pagein_pairs):
 
 
 # --------------------------------------------------------------------------------------------
+# Block K/V append  ([LX] "Three optimizations", item 1: the pool pages cold 64-token chunks to
+# host RAM bit-exact; item 3: window layers keep slot = pos mod 2048)
+# --------------------------------------------------------------------------------------------
+
+def append_full(k_new, v_new, cu_q, seq_len, cu_chunks, slot_of_chunk, host_k, host_v, k_pool, v_pool):
+    """Write the verify block's K/V rows of one full layer where later steps read them.
+
+    Block token i of sequence b sits at position p = L_b - q_b + i. Its row goes to row p mod 64
+    of chunk cu_chunks[b] + p // 64 of the chunk store ([chunk][Hkv][64][d]), and, when that
+    chunk holds a pool slot (0 <= slot_of_chunk[chunk] < slots), to the same row of the slot.
+    Writing through to the store keeps every chunk's host copy bit-exact with the pool, so a
+    chunk that leaves the pool needs no separate page-out.
+    k_new, v_new: bf16 bits [T][Hkv][d]. Returns new (host_k, host_v, k_pool, v_pool).
+    """
+    host_k, host_v = np.array(host_k, copy=True), np.array(host_v, copy=True)
+    k_pool, v_pool = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+    for b in range(len(cu_q) - 1):
+        a, e = int(cu_q[b]), int(cu_q[b + 1])
+        for i in range(e - a):
+            p = _query_position(int(seq_len[b]), e - a, i)
+            c = int(cu_chunks[b]) + p // CHUNK_TOKENS
+            r = p % CHUNK_TOKENS
+            host_k[c, :, r, :] = k_new[a + i]
+            host_v[c, :, r, :] = v_new[a + i]
+            slot = int(slot_of_chunk[c])
+            if 0 <= slot < k_pool.shape[0]:
+                k_pool[slot, :, r, :] = k_new[a + i]
+                v_pool[slot, :, r, :] = v_new[a + i]
+    return host_k, host_v, k_pool, v_pool
+
+
+def append_ring(k_new, v_new, cu_q, seq_len, ring_offset, k_ring, v_ring):
+    """Write block token i of sequence b (position p = L_b - q_b + i) into ring slot
+    (p + phi_b) mod R of every KV head of its window layer's ring ([B][Hkv][R][d]).
+    Returns new (k_ring, v_ring)."""
+    k_ring, v_ring = np.array(k_ring, copy=True), np.array(v_ring, copy=True)
+    ring_len = k_ring.shape[2]
+    for b in range(len(cu_q) - 1):
+        a, e = int(cu_q[b]), int(cu_q[b + 1])
+        for i in range(e - a):
+            p = _query_position(int(seq_len[b]), e - a, i)
+            slot = _ring_slot(p, int(ring_offset[b]), ring_len)
+            k_ring[b, :, slot, :] = k_new[a + i]
+            v_ring[b, :, slot, :] = v_new[a + i]
+    return k_ring, v_ring
+
+
+# --------------------------------------------------------------------------------------------
 # a3 + a4 + a5: masked softmax attention over an explicitly gathered key list
 # --------------------------------------------------------------------------------------------
 
