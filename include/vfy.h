@@ -10,6 +10,7 @@
  *
  *   vfy_select_resident  residency top-k over per-chunk scores + slot reconciliation
  *   vfy_page_in          bit-exact copy of newly resident chunks from pinned host memory
+ *   vfy_append_full/_swa the block's K/V rows into the chunk store, pool slot or ring
  *   vfy_attend_full      full-attention layer over the resident chunks of a KVFlash-style pool
  *   vfy_attend_swa       sliding-window layer over a position ring
  *   vfy_accept           fused argmax + greedy acceptance
@@ -209,6 +210,46 @@ VFY_API vfy_status vfy_attend_swa(vfy_ctx* ctx, const uint16_t* q, const int32_t
                                   const uint16_t* k_ring, const uint16_t* v_ring,
                                   const int32_t* ring_offset, const int32_t* seq_len,
                                   uint16_t* out, float* lse, int num_seqs, vfy_stream_t stream);
+
+/*
+ * vfy_append_full -- write the verify block's K/V rows of one full-attention layer where later
+ * steps read them. Source: "Laguna XS 2.1 33B on a RTX 3090" (lucebox), "Three optimizations"
+ * item 1 (a pool of 64-token chunks; cold chunks page to host RAM bit-exact).
+ * Block token i of sequence b sits at position p = seq_len[b] - q_b + i. Its K and V rows (all
+ * KV heads) go to row p mod 64 of chunk cu_chunks[b] + p / 64 of the chunk store and, when that
+ * chunk holds a pool slot, to the same row of the slot. Writing through to the store keeps every
+ * chunk's host copy bit-exact with the pool, so a chunk that vfy_select_resident evicts needs no
+ * page-out: its slot is simply reassigned.
+ *
+ *  k_new, v_new   bf16 [cu_q[B]][Hkv][d]   the block's K/V rows (sequence b owns rows cu_q[b]..)
+ *  cu_q, seq_len  as in vfy_attend_full
+ *  cu_chunks      int32 [B+1] (device)     sequence b's chunks are cu_chunks[b].. of the store
+ *  slot_of_chunk  int32 [cu_chunks[B]] (device)   pool slot of each chunk, -1 if not resident
+ *  host_k, host_v bf16 [num_host_chunks][Hkv][64][d]   the chunk store: pinned host memory (written
+ *                 over the host link) or device memory; outside capture, pageable memory is
+ *                 rejected with VFY_EINVAL
+ *  k_pool, v_pool bf16 [num_slots][Hkv][64][d]
+ * Pointers must be 16-byte aligned. Call it before the layer's vfy_attend_full.
+ * Device errors: a chunk index outside [0, num_host_chunks), or q_b beyond capacity: the token
+ * is skipped, VFY_EDEVICE_INPUT.
+ */
+VFY_API vfy_status vfy_append_full(vfy_ctx* ctx, const uint16_t* k_new, const uint16_t* v_new,
+                                   const int32_t* cu_q, const int32_t* seq_len, const int32_t* cu_chunks,
+                                   const int32_t* slot_of_chunk, uint16_t* host_k, uint16_t* host_v,
+                                   int64_t num_host_chunks, uint16_t* k_pool, uint16_t* v_pool,
+                                   int num_slots, int num_seqs, vfy_stream_t stream);
+
+/*
+ * vfy_append_swa -- write the verify block's K/V rows of one sliding-window layer into its ring.
+ * Source: same page, item 3 (slot = pos mod 2048, here (pos + ring_offset[b]) mod ring_len).
+ *  k_new, v_new   bf16 [cu_q[B]][Hkv][d];  cu_q, seq_len, ring_offset as in vfy_attend_swa
+ *  k_ring, v_ring bf16 [B][Hkv][ring_len][d]
+ * Call it before the layer's vfy_attend_swa.
+ * Device errors: q_b beyond capacity: the sequence's tokens are skipped, VFY_EDEVICE_INPUT.
+ */
+VFY_API vfy_status vfy_append_swa(vfy_ctx* ctx, const uint16_t* k_new, const uint16_t* v_new,
+                                  const int32_t* cu_q, const int32_t* seq_len, const int32_t* ring_offset,
+                                  uint16_t* k_ring, uint16_t* v_ring, int num_seqs, vfy_stream_t stream);
 
 /*
  * vfy_accept -- fused argmax over fp32 logits + greedy acceptance.

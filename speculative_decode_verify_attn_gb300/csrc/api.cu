@@ -250,6 +250,25 @@ vfy_status vfy_select_resident(vfy_ctx* ctx, const float* scores, const int32_t*
   return VFY_OK;
 }
 
+// Outside stream capture: check that a caller's "host" buffers are addressable by the device
+// (pinned, managed or device memory) and translate pinned host pointers to their device
+// addresses. During capture the check is skipped (the pointers are used as given).
+static vfy_status device_view(cudaStream_t s, void** ptrs, int n) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return VFY_ECUDA;
+  if (cap != cudaStreamCaptureStatusNone) return VFY_OK;
+  for (int i = 0; i < n; ++i) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return VFY_EINVAL;
+    }
+    if (a.type == cudaMemoryTypeUnregistered) return VFY_EINVAL;
+    if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) ptrs[i] = a.devicePointer;
+  }
+  return VFY_OK;
+}
+
 vfy_status vfy_page_in(vfy_ctx* ctx, const uint16_t* host_k, const uint16_t* host_v, int64_t num_host_chunks,
                        uint16_t* k_pool, uint16_t* v_pool, int num_slots, const int32_t* pagein_list,
                        const int32_t* pagein_count, int num_seqs, int k, vfy_stream_t stream) {
@@ -261,22 +280,9 @@ vfy_status vfy_page_in(vfy_ctx* ctx, const uint16_t* host_k, const uint16_t* hos
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return VFY_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // Outside stream capture, check that the host store is readable by the device (pinned,
-  // managed or device memory). During capture the check is skipped.
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  VFY_CUDA(cudaStreamIsCapturing(s, &cap));
-  const void* dev_ptr[2] = {host_k, host_v};
-  if (cap == cudaStreamCaptureStatusNone) {
-    for (int i = 0; i < 2; ++i) {
-      cudaPointerAttributes a;
-      if (cudaPointerGetAttributes(&a, dev_ptr[i]) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return VFY_EINVAL;
-      }
-      if (a.type == cudaMemoryTypeUnregistered) return VFY_EINVAL;
-      if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) dev_ptr[i] = a.devicePointer;
-    }
-  }
+  void* dev_ptr[2] = {const_cast<uint16_t*>(host_k), const_cast<uint16_t*>(host_v)};
+  const vfy_status st = device_view(s, dev_ptr, 2);
+  if (st != VFY_OK) return st;
   vfy::PageInParams p;
   p.host_k = static_cast<const uint16_t*>(dev_ptr[0]);
   p.host_v = static_cast<const uint16_t*>(dev_ptr[1]);
@@ -291,6 +297,76 @@ vfy_status vfy_page_in(vfy_ctx* ctx, const uint16_t* host_k, const uint16_t* hos
   p.chunk_elems = static_cast<long long>(ctx->cfg.num_kv_heads) * kChunk * ctx->cfg.head_dim;
   p.err = ctx->err;
   VFY_CUDA(vfy::launch_page_in(p, s));
+  ++ctx->launches;
+  return VFY_OK;
+}
+
+vfy_status vfy_append_full(vfy_ctx* ctx, const uint16_t* k_new, const uint16_t* v_new, const int32_t* cu_q,
+                           const int32_t* seq_len, const int32_t* cu_chunks, const int32_t* slot_of_chunk,
+                           uint16_t* host_k, uint16_t* host_v, int64_t num_host_chunks, uint16_t* k_pool,
+                           uint16_t* v_pool, int num_slots, int num_seqs, vfy_stream_t stream) {
+  VFY_REQUIRE(ctx != nullptr && k_new != nullptr && v_new != nullptr && cu_q != nullptr && seq_len != nullptr);
+  VFY_REQUIRE(cu_chunks != nullptr && slot_of_chunk != nullptr && host_k != nullptr && host_v != nullptr);
+  VFY_REQUIRE(k_pool != nullptr && v_pool != nullptr);
+  VFY_REQUIRE(aligned16(k_new) && aligned16(v_new) && aligned16(host_k) && aligned16(host_v) &&
+              aligned16(k_pool) && aligned16(v_pool));
+  VFY_REQUIRE(num_host_chunks >= 1 && num_host_chunks <= INT_MAX && num_slots >= 1);
+  VFY_REQUIRE(num_seqs >= 1 && num_seqs <= ctx->cfg.max_seqs);
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return VFY_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* store[2] = {host_k, host_v};
+  const vfy_status st = device_view(s, store, 2);
+  if (st != VFY_OK) return st;
+  vfy::AppendParams p = {};
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.cu_q = cu_q;
+  p.seq_len = seq_len;
+  p.num_seqs = num_seqs;
+  p.max_q = ctx->cfg.max_queries_per_seq;
+  p.token_cap = num_seqs * ctx->cfg.max_queries_per_seq;
+  p.hkv = ctx->cfg.num_kv_heads;
+  p.head_dim = ctx->cfg.head_dim;
+  p.cu_chunks = cu_chunks;
+  p.slot_of_chunk = slot_of_chunk;
+  p.host_k = static_cast<uint16_t*>(store[0]);
+  p.host_v = static_cast<uint16_t*>(store[1]);
+  p.num_host_chunks = num_host_chunks;
+  p.num_slots = num_slots;
+  p.k_dst = k_pool;
+  p.v_dst = v_pool;
+  p.err = ctx->err;
+  VFY_CUDA(vfy::launch_append(false, p, s));
+  ++ctx->launches;
+  return VFY_OK;
+}
+
+vfy_status vfy_append_swa(vfy_ctx* ctx, const uint16_t* k_new, const uint16_t* v_new, const int32_t* cu_q,
+                          const int32_t* seq_len, const int32_t* ring_offset, uint16_t* k_ring, uint16_t* v_ring,
+                          int num_seqs, vfy_stream_t stream) {
+  VFY_REQUIRE(ctx != nullptr && k_new != nullptr && v_new != nullptr && cu_q != nullptr && seq_len != nullptr);
+  VFY_REQUIRE(ring_offset != nullptr && k_ring != nullptr && v_ring != nullptr);
+  VFY_REQUIRE(aligned16(k_new) && aligned16(v_new) && aligned16(k_ring) && aligned16(v_ring));
+  VFY_REQUIRE(num_seqs >= 1 && num_seqs <= ctx->cfg.max_seqs);
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return VFY_ECUDA;
+  vfy::AppendParams p = {};
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.cu_q = cu_q;
+  p.seq_len = seq_len;
+  p.num_seqs = num_seqs;
+  p.max_q = ctx->cfg.max_queries_per_seq;
+  p.token_cap = num_seqs * ctx->cfg.max_queries_per_seq;
+  p.hkv = ctx->cfg.num_kv_heads;
+  p.head_dim = ctx->cfg.head_dim;
+  p.ring_off = ring_offset;
+  p.ring_len = ctx->cfg.ring_len;
+  p.k_dst = k_ring;
+  p.v_dst = v_ring;
+  p.err = ctx->err;
+  VFY_CUDA(vfy::launch_append(true, p, reinterpret_cast<cudaStream_t>(stream)));
   ++ctx->launches;
   return VFY_OK;
 }

@@ -135,6 +135,32 @@ struct PageInParams {
 };
 cudaError_t launch_page_in(const PageInParams& p, cudaStream_t stream);
 
+// ------------------------------ block K/V append ---------------------------------------------
+struct AppendParams {
+  const uint16_t* k_new;      // [T][Hkv][d]
+  const uint16_t* v_new;
+  const int32_t* cu_q;        // [B+1]
+  const int32_t* seq_len;     // [B]
+  int num_seqs;
+  int max_q;
+  int token_cap;              // host bound on cu_q[B]: the grid
+  int hkv, head_dim;
+  // full layers: chunk store (write-through) and pool
+  const int32_t* cu_chunks;   // [B+1]
+  const int32_t* slot_of_chunk;
+  uint16_t* host_k;           // [chunks][Hkv][64][d]
+  uint16_t* host_v;
+  long long num_host_chunks;
+  int num_slots;
+  // window layers: ring
+  const int32_t* ring_off;    // [B]
+  int ring_len;
+  uint16_t* k_dst;            // pool [slots][Hkv][64][d] or ring [B][Hkv][R][d]
+  uint16_t* v_dst;
+  int* err;
+};
+cudaError_t launch_append(bool ring, const AppendParams& p, cudaStream_t stream);
+
 // Launch with the programmatic-stream-serialization attribute so that a kernel's prologue can
 // overlap the tail of the kernel before it; every kernel calls griddepcontrol.wait before it
 // touches global memory.

@@ -15,7 +15,7 @@ VFY_OK, VFY_EINVAL, VFY_ECUDA, VFY_ENOMEM, VFY_EUNSUPPORTED, VFY_EDEVICE_INPUT, 
 
 EXPORTS = ("vfy_create", "vfy_destroy", "vfy_get_status", "vfy_strerror", "vfy_set_splits",
            "vfy_select_resident", "vfy_page_in", "vfy_attend_full", "vfy_attend_swa", "vfy_accept",
-           "vfy_accept_static", "vfy_launch_count")
+           "vfy_accept_static", "vfy_launch_count", "vfy_append_full", "vfy_append_swa")
 
 
 class VfyError(RuntimeError):
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.vfy_attend_swa.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]
         L.vfy_accept.argtypes = [_P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _P]
         L.vfy_accept_static.argtypes = [_P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P]
+        L.vfy_append_full.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P, _I, _I, _P]
+        L.vfy_append_swa.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P]
         L.vfy_launch_count.argtypes = [_P]
         L.vfy_launch_count.restype = ctypes.c_ulonglong
         for name in EXPORTS:
@@ -188,6 +190,25 @@ def vfy_page_in(ctx: Context, host_k, host_v, num_host_chunks: int, k_pool, v_po
         ctx.handle, hk, hv, num_host_chunks, _dev(k_pool, BF16, "k_pool"), _dev(v_pool, BF16, "v_pool"),
         num_slots, _dev(pagein_list, I32, "pagein_list"), _dev(pagein_count, I32, "pagein_count"),
         num_seqs, k, _stream(stream)), "vfy_page_in")
+
+
+def vfy_append_full(ctx: Context, k_new, v_new, cu_q, seq_len, cu_chunks, slot_of_chunk, host_k, host_v,
+                    num_host_chunks: int, k_pool, v_pool, num_slots: int, num_seqs: int, stream=None):
+    hk = _dev(host_k, BF16, "host_k") if host_k.is_cuda else _host(host_k, BF16, "host_k")
+    hv = _dev(host_v, BF16, "host_v") if host_v.is_cuda else _host(host_v, BF16, "host_v")
+    _check(lib().vfy_append_full(
+        ctx.handle, _dev(k_new, BF16, "k_new"), _dev(v_new, BF16, "v_new"), _dev(cu_q, I32, "cu_q"),
+        _dev(seq_len, I32, "seq_len"), _dev(cu_chunks, I32, "cu_chunks"), _dev(slot_of_chunk, I32, "slot_of_chunk"),
+        hk, hv, num_host_chunks, _dev(k_pool, BF16, "k_pool"), _dev(v_pool, BF16, "v_pool"), num_slots, num_seqs,
+        _stream(stream)), "vfy_append_full")
+
+
+def vfy_append_swa(ctx: Context, k_new, v_new, cu_q, seq_len, ring_offset, k_ring, v_ring, num_seqs: int,
+                   stream=None):
+    _check(lib().vfy_append_swa(
+        ctx.handle, _dev(k_new, BF16, "k_new"), _dev(v_new, BF16, "v_new"), _dev(cu_q, I32, "cu_q"),
+        _dev(seq_len, I32, "seq_len"), _dev(ring_offset, I32, "ring_offset"), _dev(k_ring, BF16, "k_ring"),
+        _dev(v_ring, BF16, "v_ring"), num_seqs, _stream(stream)), "vfy_append_swa")
 
 
 def vfy_attend_full(ctx: Context, q, cu_q, k_pool, v_pool, num_slots: int, resident_ids, resident_slots,
