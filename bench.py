@@ -513,6 +513,13 @@ def run_ours(args):
         c_mean, _, _ = event_time_graph(g_acc, flush, k_steps)
         g_pg = capture(vp.enqueue_paging)
         p_mean, _, _ = event_time_graph(g_pg, flush, min(k_steps, 100), pre=next_scores)
+        # the pass with the block's K/V rows appended in every layer (full layers write through to
+        # the pinned chunk store): block KV append inside the graph
+        g_app = vp.capture(append=True)
+        ap_mean, _, _ = event_time_graph(g_app, flush, k_steps, pre=next_scores)
+        extras["pass_with_append"] = {"us_per_layer": round(ap_mean * 1000 / sz.n_layers, 3),
+                                      "kernels": vp.kernels_per_pass_append}
+        del g_app
         pg_bytes = len(vp.full_layers) * wl.pagein_per_step * vp.shape.num_kv_heads * 64 * vp.shape.head_dim * 4
         extras["layers_only_us_per_layer"] = round(l_mean * 1000 / sz.n_layers, 3)
         extras["layers_only_kv_gbs"] = round((sz.bytes_pass - sz.bytes_accept) / (l_mean * 1e-3) / 1e9, 1)

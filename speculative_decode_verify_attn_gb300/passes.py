@@ -155,6 +155,8 @@ class VerifyPass:
         self.outs = [self.out_all[l] for l in range(self.n_layers)]
         self.lse_all = torch.empty((self.n_layers, self.q, hq), device=dev, dtype=torch.float32)
         self.lses = [self.lse_all[l] for l in range(self.n_layers)]
+        # the block's own K/V rows of every layer (for passes that append them before attending)
+        self.kv_new = torch.randn((self.n_layers, 2, self.q, hkv, d), generator=gen, device=dev, dtype=torch.bfloat16)
         # --- acceptance ---
         targets = rng.integers(0, self.vocab, self.q)
         self.targets = targets
@@ -172,6 +174,7 @@ class VerifyPass:
         self.side = torch.cuda.Stream(device=dev, priority=-1)
         self.graph = None
         self.kernels_per_pass = None
+        self.kernels_per_pass_append = None
         self.step = 0
 
     # ------------------------------------------------------------------------------------------
@@ -231,8 +234,24 @@ class VerifyPass:
         vfy.vfy_accept(self.ctx, self.logits, self.vocab, self.drafts, self.cu_rows, self.q, self.accepted,
                        self.bonus, self.committed, 1, torch.cuda.current_stream(self.dev))
 
-    def enqueue(self):
-        """Enqueue one pass on the current stream (used for capture and for eager runs)."""
+    def append_layer(self, l: int, stream=None):
+        """The block's K/V rows of layer l into its pool slot and chunk store (written through
+        to pinned host memory) or into its ring."""
+        kn, vn = self.kv_new[l, 0], self.kv_new[l, 1]
+        if is_full_layer(l):
+            vfy.vfy_append_full(self.ctx, kn, vn, self.cu_q, self.seq_len, self.cu_chunks, self.slot_of_chunk,
+                                self.host_k[l] if self.host_k else self.pool_k[l],
+                                self.host_v[l] if self.host_v else self.pool_v[l],
+                                self.n_chunks if self.host_k else self.k, self.pool_k[l], self.pool_v[l], self.k, 1,
+                                stream)
+        else:
+            vfy.vfy_append_swa(self.ctx, kn, vn, self.cu_q, self.seq_len, self.ring_offset, self.ring_k[l],
+                               self.ring_v[l], 1, stream)
+
+    def enqueue(self, append: bool = False):
+        """Enqueue one pass on the current stream (used for capture and for eager runs). With
+        append, every layer first writes the block's own K/V rows (block KV append inside the
+        graph); without, they are a precondition of the pass."""
         main = torch.cuda.current_stream(self.dev)
         events = {}
         joins = {}
@@ -259,27 +278,39 @@ class VerifyPass:
             if is_full_layer(l):
                 if fi in joins:
                     main.wait_event(events[self.full_layers[joins[fi]]])
+                if append:
+                    self.append_layer(l, main)
                 self.attend_full_layer(l, main)
                 fi += 1
             else:
+                if append:
+                    self.append_layer(l, main)
                 self.attend_swa_layer(l, main)
         vfy.vfy_accept(self.ctx, self.logits, self.vocab, self.drafts, self.cu_rows, self.q, self.accepted,
                        self.bonus, self.committed, 1, main)
         if not self.all_resident:
             main.wait_stream(self.side)
 
-    def capture(self):
+    def capture(self, append: bool = False):
+        """Capture the pass as self.graph (with append, the variant that appends the block's
+        K/V rows in every layer; its kernel count goes to kernels_per_pass_append)."""
         # one eager pass first (also sets kernel attributes outside capture)
-        self.set_step_scores(0)
-        self.enqueue()
+        self.set_step_scores(self.step)
+        self.enqueue(append)
         torch.cuda.synchronize(self.dev)
-        self.graph = torch.cuda.CUDAGraph()
+        graph = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
         n0 = vfy.vfy_launch_count(self.ctx)
         with torch.cuda.stream(s):
-            with torch.cuda.graph(self.graph, stream=s):
-                self.enqueue()
+            with torch.cuda.graph(graph, stream=s):
+                self.enqueue(append)
+        if append:
+            self.kernels_per_pass_append = vfy.vfy_launch_count(self.ctx) - n0
+            torch.cuda.current_stream(self.dev).wait_stream(s)
+            torch.cuda.synchronize(self.dev)
+            return graph
+        self.graph = graph
         self.kernels_per_pass = vfy.vfy_launch_count(self.ctx) - n0
         torch.cuda.current_stream(self.dev).wait_stream(s)
         torch.cuda.synchronize(self.dev)

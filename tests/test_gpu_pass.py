@@ -106,3 +106,41 @@ def test_all_resident_256k_layer_sampled():
             assert abs(glse[i, g] - rlse[i, g]) <= 2e-3 + 1e-3 * abs(rlse[i, g])
     finally:
         ar.close()
+
+
+def test_pass_with_block_kv_append(pass256k):
+    """The pass variant that appends the block's K/V rows in every layer before attending (full
+    layers write through to the pinned chunk store): after one replay, the block rows of a full
+    layer's pool and chunk store and of a window layer's ring are the oracle's, bit for bit, and
+    both layers' outputs match the oracle on the updated data."""
+    vp = pass256k
+    g = vp.capture(append=True)
+    lf, ls = vp.full_layers[2], vp.swa_layers[7]
+    # the state the replay starts from (the capture's eager run already appended once; appending
+    # the same rows again is idempotent)
+    prev = vp.slot_of_chunk.cpu().numpy().copy()
+    scores = vp.score_table[vp.step % vp.score_table.shape[0]].cpu().numpy()
+    vp.set_step_scores(vp.step)
+    vp.step += 1
+    g.replay()
+    torch.cuda.synchronize()
+    ref_sel = O.select_resident(scores, [0, vp.n_chunks], vp.k, prev)
+    soc = ref_sel["slot_of_chunk"]
+    kn, vn = bits(vp.kv_new[lf, 0]), bits(vp.kv_new[lf, 1])
+    cu_q, lens = [0, vp.q], [vp.L]
+    hk, hv, pk, pv = bits(vp.host_k[lf]), bits(vp.host_v[lf]), bits(vp.pool_k[lf]), bits(vp.pool_v[lf])
+    ek, ev, epk, epv = O.append_full(kn, vn, cu_q, lens, [0, vp.n_chunks], soc, hk, hv, pk, pv)
+    assert np.array_equal(hk, ek) and np.array_equal(hv, ev)       # the rows are already in place
+    assert np.array_equal(pk, epk) and np.array_equal(pv, epv)
+    ids, slots = ref_sel["resident_ids"], ref_sel["resident_slots"]
+    ref, rlse = O.attend_full_seq(bits(vp.qs[lf]), pk, pv, ids, slots, vp.L)
+    assert_attn_close(bits(vp.outs[lf]), ref, f"full layer {lf} with append")
+    assert_lse_close(vp.lses[lf].cpu().numpy(), rlse, f"full layer {lf} with append")
+    kr, vr = bits(vp.ring_k[ls]), bits(vp.ring_v[ls])
+    ekr, evr = O.append_ring(bits(vp.kv_new[ls, 0]), bits(vp.kv_new[ls, 1]), cu_q, lens,
+                             [int(vp.ring_offset.item())], kr, vr)
+    assert np.array_equal(kr, ekr) and np.array_equal(vr, evr)
+    ref, rlse = O.attend_ring_seq(bits(vp.qs[ls]), kr[0], vr[0], int(vp.ring_offset.item()), vp.L, synth.WINDOW)
+    assert_attn_close(bits(vp.outs[ls]), ref, f"window layer {ls} with append")
+    assert_lse_close(vp.lses[ls].cpu().numpy(), rlse, f"window layer {ls} with append")
+    assert vp.kernels_per_pass_append == vp.launches_per_step() + vp.n_layers
