@@ -185,6 +185,40 @@ def page_in(host_k, host_v, k_pool, v_pool, pagein_pairs):
 
 
 # --------------------------------------------------------------------------------------------
+# Confidence-gated draft depths  ([WD] "Width vs. Depth: Speculating on the Margin": draft depth
+# allocated unevenly by drafter confidence beats fixed depths; it needs ragged speculation)
+# --------------------------------------------------------------------------------------------
+
+def expected_committed(confidence: float, depth: int) -> float:
+    """Expected tokens one verify step commits for a sequence whose drafted positions are each
+    accepted with probability c, independently: the accepted prefix plus the bonus token,
+    1 + c + c^2 + ... + c^depth."""
+    return sum(confidence ** k for k in range(depth + 1))
+
+
+def gate_depths(confidence, row_budget: int, max_depth: int) -> list[int]:
+    """Draft depths D_b that maximise the expected committed tokens sum_b expected_committed(c_b,
+    D_b) under a budget of verify rows sum_b (D_b + 1) <= row_budget and 0 <= D_b <= max_depth.
+    Adding one drafted position to sequence b gains c_b^(D_b + 1), which shrinks as D_b grows,
+    so handing out the rows one at a time to the largest gain (ties to the lower index) reaches
+    the maximum. Every sequence keeps its one row for the committed token."""
+    depth = [0] * len(confidence)
+    rows = len(confidence)
+    while rows < row_budget:
+        best, gain = -1, -1.0
+        for b, c in enumerate(confidence):
+            if depth[b] < max_depth:
+                g = float(c) ** (depth[b] + 1)
+                if g > gain:
+                    best, gain = b, g
+        if best < 0:
+            break
+        depth[best] += 1
+        rows += 1
+    return depth
+
+
+# --------------------------------------------------------------------------------------------
 # Block K/V append  ([LX] "Three optimizations", item 1: the pool pages cold 64-token chunks to
 # host RAM bit-exact; item 3: window layers keep slot = pos mod 2048)
 # --------------------------------------------------------------------------------------------
