@@ -355,6 +355,64 @@ def prefill_shaped_point(vp, flush, local, rank, steps, tf_peak):
             "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / tf_peak, 4) if tf_peak else None}
 
 
+def depth_policy_point(flush, local, rank, steps):
+    """Confidence-gated draft depths against a fixed depth on the ragged batch (8 sequences,
+    contexts on [4000, 200000], 16 q / 4 KV heads x 128). Per-sequence acceptance probabilities
+    are drawn from Beta(2.8, 2.2) (mean 0.56, the pages' acceptance rate). The fixed policy drafts
+    8 tokens per sequence (72 verify rows); the gated one spends the same 72 rows by
+    vfy_gate_depths. Expected committed tokens per step: 1 + c + ... + c^D per sequence. The
+    verify step is timed on the kernels: one all-resident global layer and one window layer for
+    each depth vector, scaled to 12 global + 36 window layers."""
+    import numpy as np
+    import torch
+
+    from speculative_decode_verify_attn_gb300 import synth, vfy
+    w = synth.workload_ragged(0)
+    s = w.shape
+    B = w.num_seqs
+    rng = np.random.default_rng(rank + 31)
+    conf = rng.beta(2.8, 2.2, B).astype(np.float32)
+    fixed = [8] * B
+    budget = sum(d + 1 for d in fixed)
+    gated = vfy.vfy_gate_depths(conf, budget, synth.DRAFT)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(rank + 31)
+    n_per = [(L + 63) // 64 for L in w.seq_lens]
+    total = sum(n_per)
+    kp = torch.randn((total, s.num_kv_heads, 64, s.head_dim), generator=gen, device="cuda", dtype=torch.bfloat16)
+    vp_ = torch.randn_like(kp)
+    kr = torch.randn((B, s.num_kv_heads, synth.RING, s.head_dim), generator=gen, device="cuda", dtype=torch.bfloat16)
+    vr = torch.randn_like(kr)
+    i32 = lambda a: torch.tensor(np.asarray(a, dtype=np.int32), dtype=torch.int32, device="cuda")
+    ids = i32(np.concatenate([np.arange(n) for n in n_per]))
+    slots = i32(rng.permutation(total))
+    cu_res = i32(np.concatenate([[0], np.cumsum(n_per)]))
+    seq_len = i32(w.seq_lens)
+    phis = i32([synth.wrapping_ring_offset(rng, L, synth.WINDOW + 16, synth.RING) for L in w.seq_lens])
+    ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, max_seqs=B, max_queries_per_seq=synth.DRAFT + 1,
+                         device=local)
+    out = {"sequences": B, "confidence_mean": round(float(conf.mean()), 3), "row_budget": budget}
+    for name, depths in (("fixed", fixed), ("gated", gated)):
+        qs = [d + 1 for d in depths]
+        cu_q = i32(np.concatenate([[0], np.cumsum(qs)]))
+        q = torch.randn((sum(qs), s.num_q_heads, s.head_dim), generator=gen, device="cuda", dtype=torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty((sum(qs), s.num_q_heads), dtype=torch.float32, device="cuda")
+        g_full = capture(lambda: vfy.vfy_attend_full(ctx, q, cu_q, kp, vp_, total, ids, slots, cu_res, max(n_per),
+                                                     seq_len, o, lse, B))
+        t_full, _, _ = event_time_graph(g_full, flush, steps)
+        g_win = capture(lambda: vfy.vfy_attend_swa(ctx, q, cu_q, kr, vr, phis, seq_len, o, lse, B))
+        t_win, _, _ = event_time_graph(g_win, flush, steps)
+        del g_full, g_win
+        step_us = 1000 * (12 * t_full + 36 * t_win)
+        tokens = float(sum(sum(float(c) ** k for k in range(d + 1)) for c, d in zip(conf, depths)))
+        out[name] = {"depths": depths, "tokens_per_step": round(tokens, 3), "step_us": round(step_us, 1),
+                     "tokens_per_s": round(tokens / (step_us * 1e-6), 1)}
+    out["gated_over_fixed"] = round(out["gated"]["tokens_per_s"] / out["fixed"]["tokens_per_s"], 4)
+    ctx.close()
+    return out
+
+
 def drafter_ring_point(flush, local, rank, steps, peak):
     """The drafter's context-KV ring: the 5 layers of the drafter head attend a 4096-position
     window in an 8192-slot ring (16 proposals, 256K context, a wrapping write head), one graph.
@@ -546,6 +604,7 @@ def run_ours(args):
         extras["drafter_ring"] = drafter_ring_point(flush, local, rank, max(20, min(args.steps, 500)), peak)
         extras["prefill_shaped_verify"] = prefill_shaped_point(vp, flush, local, rank, max(20, min(args.steps, 200)),
                                                                bf16_peak())
+        extras["depth_policy"] = depth_policy_point(flush, local, rank, max(20, min(args.steps, 100)))
 
     # end to end: inputs host->device from pinned memory, accepted tokens back, inside the timing
     e2e = None

@@ -252,6 +252,20 @@ VFY_API vfy_status vfy_append_swa(vfy_ctx* ctx, const uint16_t* k_new, const uin
                                   uint16_t* k_ring, uint16_t* v_ring, int num_seqs, vfy_stream_t stream);
 
 /*
+ * vfy_gate_depths -- confidence-gated draft depths for a ragged verify batch (host function, no
+ * device work, no context). Source: "Width vs. Depth: Speculating on the Margin" (draft depth
+ * allocated unevenly by drafter confidence beats fixed depths; it needs ragged speculation).
+ * Sequence b's drafted positions are each accepted with probability confidence[b] in [0, 1],
+ * independently, so depth D commits 1 + c + ... + c^D tokens in expectation. The depths
+ * maximise that sum under sum_b (depths[b] + 1) <= row_budget and 0 <= depths[b] <= max_depth
+ * (rows are handed out one at a time to the largest gain c^(D+1), ties to the lower index).
+ *  confidence  fp32 [num_seqs] host;  depths  int32 [num_seqs] host, OUT
+ * Returns VFY_EINVAL for a confidence outside [0, 1] (or NaN) or a negative count.
+ */
+VFY_API vfy_status vfy_gate_depths(const float* confidence, int num_seqs, int row_budget, int max_depth,
+                                   int32_t* depths);
+
+/*
  * vfy_accept -- fused argmax over fp32 logits + greedy acceptance.
  * Source: same page, "The model ..." (commit only tokens the target itself would emit) and
  * "The Death of the Compute-Moat", "DFlash Drafters ..." (verify, commit, fallback).

@@ -15,7 +15,8 @@ VFY_OK, VFY_EINVAL, VFY_ECUDA, VFY_ENOMEM, VFY_EUNSUPPORTED, VFY_EDEVICE_INPUT, 
 
 EXPORTS = ("vfy_create", "vfy_destroy", "vfy_get_status", "vfy_strerror", "vfy_set_splits",
            "vfy_select_resident", "vfy_page_in", "vfy_attend_full", "vfy_attend_swa", "vfy_accept",
-           "vfy_accept_static", "vfy_launch_count", "vfy_append_full", "vfy_append_swa")
+           "vfy_accept_static", "vfy_launch_count", "vfy_append_full", "vfy_append_swa",
+           "vfy_gate_depths")
 
 
 class VfyError(RuntimeError):
@@ -64,6 +65,7 @@ def lib() -> ctypes.CDLL:
         L.vfy_accept_static.argtypes = [_P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P]
         L.vfy_append_full.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P, _I, _I, _P]
         L.vfy_append_swa.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P]
+        L.vfy_gate_depths.argtypes = [_P, _I, _I, _I, _P]
         L.vfy_launch_count.argtypes = [_P]
         L.vfy_launch_count.restype = ctypes.c_ulonglong
         for name in EXPORTS:
@@ -165,6 +167,17 @@ def vfy_get_status(ctx: Context, stream=None) -> int:
 
 def vfy_launch_count(ctx: Context) -> int:
     return int(lib().vfy_launch_count(ctx.handle))
+
+
+def vfy_gate_depths(confidence, row_budget: int, max_depth: int) -> list[int]:
+    """Host function (no device): confidence-gated draft depths. `confidence` is a sequence of
+    per-sequence acceptance probabilities in [0, 1]."""
+    import numpy as _np
+    c = _np.ascontiguousarray(_np.asarray(confidence, dtype=_np.float32))
+    d = _np.zeros(len(c), dtype=_np.int32)
+    _check(lib().vfy_gate_depths(c.ctypes.data_as(_P), len(c), int(row_budget), int(max_depth),
+                                 d.ctypes.data_as(_P)), "vfy_gate_depths")
+    return d.tolist()
 
 
 def vfy_set_splits(ctx: Context, full_splits: int = 0, swa_splits: int = 0):

@@ -35,3 +35,28 @@ def test_gate_depths_special_cases():
     assert O.gate_depths([0.5, 0.5], 5, 16) == [2, 1]                    # ties go to the lower index
     assert O.gate_depths([0.7, 0.7, 0.7], 30, 4) == [4, 4, 4]            # budget beyond every max
     assert O.gate_depths([], 4, 2) == []
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_library_gate_depths_matches_the_oracle(seed):
+    """vfy_gate_depths (host code of libvfy.so, no device needed) gives the oracle's depths."""
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decode_verify_attn_gb300 import vfy
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(0, 12))
+    conf = rng.uniform(0, 1, n).astype(np.float32)
+    if n > 2:
+        conf[1] = conf[0]                                  # a tie
+    max_depth = int(rng.integers(0, 17))
+    budget = int(rng.integers(0, n * 18 + 2))
+    assert vfy.vfy_gate_depths(conf, budget, max_depth) == O.gate_depths([float(c) for c in conf], budget, max_depth)
+
+
+def test_library_gate_depths_rejects_bad_confidence():
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decode_verify_attn_gb300 import vfy
+    for bad in ([0.5, float("nan")], [1.5], [-0.1]):
+        with pytest.raises(vfy.VfyError):
+            vfy.vfy_gate_depths(bad, 10, 4)
