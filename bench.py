@@ -50,6 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-extras", action="store_true", help="skip the all-resident and per-kernel points")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host copies) measurement")
     ap.add_argument("--oracle-sample", type=float, default=0.0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-steps", default="", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -168,10 +169,10 @@ def bf16_peak():
 # CPU oracle sample (one host core)
 # ---------------------------------------------------------------------------------------------
 
-def oracle_sample_seconds(budget_s: float) -> dict:
-    """Time the fp64 oracle on one full layer (8K resident of 4096 chunks), one window layer,
-    the residency selection, 16 page-ins and the acceptance, repeated for about budget_s; scale
-    to the 40-layer pass (10 full + 30 window)."""
+def _oracle_rep_fn():
+    """Build the oracle sample's inputs once and return a function that runs one repetition of
+    it: one full layer (8K resident of 4096 chunks), one window layer, the residency selection,
+    16 page-ins and the acceptance. It returns the seconds each part took."""
     import numpy as np
 
     from oracle import vfy_oracle as O
@@ -195,10 +196,8 @@ def oracle_sample_seconds(budget_s: float) -> dict:
     targets = rng.integers(0, synth.VOCAB, q)
     logits = synth.planted_logits(rng, targets, synth.VOCAB)
     drafts = synth.drafts_matching(rng, targets, 0.56, synth.VOCAB)
-    t = {"select": [], "page_in": [], "full": [], "swa": [], "accept": []}
-    t_end = time.perf_counter() + budget_s
-    reps = 0
-    while reps < 1 or time.perf_counter() < t_end:
+
+    def rep() -> dict:
         a = time.perf_counter()
         res = O.select_resident(scores, [0, n], k, res0["slot_of_chunk"])
         b = time.perf_counter()
@@ -211,22 +210,55 @@ def oracle_sample_seconds(budget_s: float) -> dict:
         e = time.perf_counter()
         O.accept(logits, drafts, [0, q])
         f = time.perf_counter()
-        for key, dt in zip(t, (b - a, c - b, d - c, e - d, f - e)):
+        return dict(zip(("select", "page_in", "full", "swa", "accept"), (b - a, c - b, d - c, e - d, f - e)))
+
+    return rep
+
+
+def _pass_seconds(m: dict) -> float:
+    """Scale one repetition's parts to the 40-layer pass: 10 full + 30 window layers."""
+    return m["select"] + 10 * m["page_in"] + 10 * m["full"] + 30 * m["swa"] + m["accept"]
+
+
+def oracle_sample_seconds(budget_s: float) -> dict:
+    """Repeat the oracle sample for about budget_s (at least once); mean us per layer."""
+    rep = _oracle_rep_fn()
+    t = {"select": [], "page_in": [], "full": [], "swa": [], "accept": []}
+    t_end = time.perf_counter() + budget_s
+    reps = 0
+    while reps < 1 or time.perf_counter() < t_end:
+        for key, dt in rep().items():
             t[key].append(dt)
         reps += 1
     m = {key: statistics.mean(v) for key, v in t.items()}
-    pass_s = m["select"] + 10 * m["page_in"] + 10 * m["full"] + 30 * m["swa"] + m["accept"]
+    pass_s = _pass_seconds(m)
     return {"us_per_layer": pass_s * 1e6 / 40, "reps": reps, "parts_s": m, "pass_s": pass_s}
 
 
-def run_oracle_child(budget_s: float) -> dict:
-    """Run the oracle sample in a child process pinned to one BLAS / OpenMP thread."""
+def oracle_steps(warm: int, steps: int, budget_s: float) -> dict:
+    """The reference arm's loop, in one process: `warm` untimed repetitions, then up to `steps`
+    timed ones, stopping early once budget_s of timed work has run (at least one step). Each
+    step is one repetition scaled to the pass; returns every step's us per layer."""
+    rep = _oracle_rep_fn()
+    for _ in range(warm):
+        rep()
+    vals = []
+    t0 = time.perf_counter()
+    while len(vals) < steps and (not vals or time.perf_counter() - t0 < budget_s):
+        vals.append(_pass_seconds(rep()) * 1e6 / 40)
+    return {"warmup": warm, "steps": len(vals), "us_per_layer": vals, "timed_s": time.perf_counter() - t0}
+
+
+def run_oracle_child(budget_s: float, steps_spec: str = "") -> dict:
+    """Run the oracle sample (or the reference arm's loop, with steps_spec "W,K,budget") in a
+    child process pinned to one BLAS / OpenMP thread."""
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[var] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", str(budget_s)],
-                         capture_output=True, text=True, env=env, cwd=ROOT)
+    cmd = [sys.executable, os.path.abspath(__file__)]
+    cmd += ["--oracle-steps", steps_spec] if steps_spec else ["--oracle-sample", str(budget_s)]
+    out = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT)
     if out.returncode != 0:
         raise RuntimeError("oracle sample failed:\n" + out.stderr[-2000:])
     return json.loads(out.stdout.strip().splitlines()[-1])
@@ -243,30 +275,34 @@ def cpu_baseline_obj(res: dict) -> dict:
 # Reference arm: the oracle, as it stands, on the host cores
 # ---------------------------------------------------------------------------------------------
 
+REFERENCE_WARMUP = (3, 5)       # the reference arm's warm-up steps: at least 3, at most 5
+REFERENCE_BUDGET_S = 120.0      # timed oracle work at most (about 1.3 s a step on one core)
+
+
 def run_reference(args):
     rank, local, world = dist_info()
     if rank != 0:
         return 0
-    steps = max(1, min(args.steps, 40))
-    warm = min(args.warmup, 2)
-    for _ in range(warm):
-        run_oracle_child(0.0)
-    vals = []
+    warm = min(max(args.warmup, REFERENCE_WARMUP[0]), REFERENCE_WARMUP[1])
+    steps = max(1, args.steps)
     t0 = time.perf_counter()
-    last = None
-    for _ in range(steps):
-        last = run_oracle_child(0.0)
-        vals.append(last["us_per_layer"])
+    res = run_oracle_child(0.0, f"{warm},{steps},{REFERENCE_BUDGET_S}")
     wall = time.perf_counter() - t0
+    vals = res["us_per_layer"]
     value = statistics.mean(vals)
+    sample = (f"fp64 numpy oracle, one thread; each step: 1 full layer (128 of 4096 chunks resident, 17 queries "
+              f"x 16 heads), 1 window layer, residency top-128 of 4096, 16 page-ins, accept over 17 x 131072, "
+              f"scaled to 10 full + 30 window layers per pass / 40")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
-            "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": round(value * 40 / 1000, 3),
+            "n_gpus": args.gpus, "steps": res["steps"], "warmup": res["warmup"],
+            "ms_per_step": round(value * 40 / 1000, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": "verify pass, 256K context, 16-token draft (sampled on the CPU)",
-                       "steps_capped_at": 40, "wall_s": round(wall, 2)},
+                       "steps_requested": args.steps, "timed_budget_s": REFERENCE_BUDGET_S,
+                       "wall_s": round(wall, 2)},
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": cpu_baseline_obj(last)["sample"]},
+                             "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -641,6 +677,10 @@ def run_ours(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.oracle_steps:
+        w, k, budget = args.oracle_steps.split(",")
+        print(json.dumps(oracle_steps(int(w), int(k), float(budget))))
+        return 0
     if args.oracle_sample or "--oracle-sample" in (argv or sys.argv):
         print(json.dumps(oracle_sample_seconds(args.oracle_sample)))
         return 0

@@ -72,6 +72,8 @@ def test_reference_arm_prints_its_line():
     assert line["metric"] == bench.METRIC
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+    # at least 3 untimed warm-up steps, whatever was asked; the timed steps asked for, within the budget
+    assert line["warmup"] >= 3 and line["steps"] == 1
 
 
 def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
