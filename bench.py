@@ -10,7 +10,9 @@ rate), captured once as a CUDA graph and replayed. Inputs are synthetic and seed
 One JSON line on stdout (rank 0):
   metric/unit   verify-attention microseconds per layer (lower is better), whole pass / 40 layers,
                 KV GB/s and the fraction of measured HBM bandwidth reported beside it
-  value         device time of the graph replay, L2 flushed (256 MiB write) between steps
+  value         device time of the graph replay; between steps the L2 is flushed by writing a
+                256 MiB buffer and then reading it back, so each step starts with an L2 that
+                holds none of its inputs and no dirty lines
   e2e           the same, with the step's inputs copied host->device from pinned memory and the
                 accepted tokens copied back inside the timed region
   roofline      for the dominant kernel (full-layer attention): algorithmic bytes / event time
@@ -35,6 +37,29 @@ if ROOT not in sys.path:
 METRIC = "verify-attn µs/layer and KV GB/s (% of HBM peak) at 256K ctx, 16-token draft"
 UNIT = "us/layer"
 FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Evicts the L2 (129 MB) between timed steps: write a buffer twice its size, then (clean)
+    read it back with a reduction. The write alone would leave the L2 full of dirty lines whose
+    write-back then falls inside the next timed region (about 129 MB of HBM writes, 19 us at
+    full bandwidth); the read evicts them before the timing starts."""
+
+    def __init__(self, nbytes: int, clean: bool = True, buf=None):
+        import torch
+        self.buf = buf if buf is not None else torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+        self.out = torch.empty((), dtype=torch.float32, device="cuda")
+        self.clean = clean
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        if self.clean:
+            torch.sum(self.buf, 0, out=self.out)
+
+    def dirty(self) -> "L2Flush":
+        """The same buffer, write-only (the L2 left full of dirty lines)."""
+        return L2Flush(0, clean=False, buf=self.buf)
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -313,14 +338,14 @@ def run_reference(args):
 # ---------------------------------------------------------------------------------------------
 
 def event_time_graph(graph, flush, steps, pre=None):
-    """Mean / median device time (ms) of graph replays, L2 flushed before each."""
+    """Mean / median device time (ms) of graph replays, L2 flushed (`flush()`) before each."""
     import torch
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
         if pre is not None:
             pre(i)
-        flush.zero_()
+        flush()
         starts[i].record()
         graph.replay()
         ends[i].record()
@@ -524,7 +549,7 @@ def measure_e2e(vp, flush, args, local, sz, world):
         # this step's residency scores, written into the pinned input image on the host
         in_host.narrow(0, s_off, score_view.numel()).copy_(score_host[vp.step % len(score_host)])
         vp.step += 1
-        flush.zero_()
+        flush()
         starts[i].record()
         vp.inputs.copy_(in_host, non_blocking=True)
         vp.replay()
@@ -554,13 +579,13 @@ def run_ours(args):
     vp = passes.VerifyPass(wl, device=local, seed=rank)
     sz = vp.sizes()
     vp.capture()
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush(FLUSH_BYTES)
 
     # warm-up: steady-state residency (16 new chunks per step)
     for i in range(max(args.warmup, 3)):
         vp.set_step_scores(vp.step)
         vp.step += 1
-        flush.zero_()
+        flush()
         vp.replay()
     torch.cuda.synchronize()
 
@@ -635,6 +660,12 @@ def run_ours(args):
         extras["all_resident_256k_layer"] = {"us": round(a_mean * 1000, 2), "bytes": a_bytes,
                                              "gbs": round(a_bytes / (a_mean * 1e-3) / 1e9, 1),
                                              "frac": round(a_bytes / (a_mean * 1e-3) / 1e9 / peak, 4)}
+        # the same two graphs with the write-only flush: the L2 starts each step full of dirty lines
+        dflush = flush.dirty()
+        d_ar, _, _ = event_time_graph(g_ar, dflush, max(20, min(args.steps, 200)))
+        d_pass, _, _ = event_time_graph(vp.graph, dflush, min(args.steps, 500), pre=next_scores)
+        extras["write_only_l2_flush"] = {"pass_us_per_layer": round(d_pass * 1000 / sz.n_layers, 3),
+                                         "all_resident_256k_layer_us": round(d_ar * 1000, 2)}
         del g_ar
         ar.close()
         extras["drafter_ring"] = drafter_ring_point(flush, local, rank, max(20, min(args.steps, 500)), peak)
@@ -661,7 +692,7 @@ def run_ours(args):
                 "config": {"workload": wl.name, "seq_len": wl.seq_lens[0], "draft": wl.depths[0],
                            "layers": sz.n_layers, "full_layers": sz.n_full, "window_layers": sz.n_swa,
                            "resident_chunks": wl.resident_chunks, "pagein_per_step": wl.pagein_per_step,
-                           "heads": "16q/4kv x 128", "l2": "flushed between steps (256 MiB write)",
+                           "heads": "16q/4kv x 128", "l2": "flushed between steps (256 MiB write, then read back)",
                            "parallelism": f"replicas x{world}", "timing": "CUDA events around each graph replay"},
                 "kv_gbs": round(kv_gbs, 1), "kv_frac_of_hbm": round(kv_gbs / peak, 4),
                 "median_ms_per_step": round(med_ms, 5), "wall_s": round(wall, 3),
