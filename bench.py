@@ -531,9 +531,11 @@ def capture(fn):
 
 
 def measure_e2e(vp, flush, args, local, sz, world):
-    """The pass through the C ABI from host buffers: each step copies its inputs (block queries of
-    all layers, residency scores, logits, drafts) from pinned host memory in one copy, replays the
-    pass, and reads its results (accepted length, bonus, committed tokens) back in one copy."""
+    """The pass through the C ABI from host buffers: each step copies its inputs (residency
+    scores, block queries of all layers, logits, drafts) from pinned host memory, runs the pass and
+    copies its results (accepted length, bonus, committed tokens) back to pinned host memory, all
+    in one captured graph per step. The queries of later layers and the logits arrive on a copy
+    stream while the first layers run (VerifyPass.enqueue_end_to_end)."""
     import torch
     in_host = vp.inputs.cpu().pin_memory()
     score_view = vp.scores.view(torch.uint8)
@@ -542,26 +544,30 @@ def measure_e2e(vp, flush, args, local, sz, world):
     out_host = torch.empty(vp.results.numel(), dtype=torch.int32).pin_memory()
     h2d = in_host.numel()
     d2h = out_host.numel() * 4
+    g = vp.capture_end_to_end(in_host, out_host)
     e_steps = max(20, min(args.steps, 500))
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
-    for i in range(e_steps):
+    for i in range(-3, e_steps):
         # this step's residency scores, written into the pinned input image on the host
         in_host.narrow(0, s_off, score_view.numel()).copy_(score_host[vp.step % len(score_host)])
         vp.step += 1
         flush()
+        if i < 0:                      # warm-up replays
+            g.replay()
+            torch.cuda.synchronize()
+            continue
         starts[i].record()
-        vp.inputs.copy_(in_host, non_blocking=True)
-        vp.replay()
-        out_host.copy_(vp.results, non_blocking=True)
+        g.replay()
         ends[i].record()
         ends[i].synchronize()
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
     e2e_ms = dist_max(e2e_ms, torch.device("cuda", local))
-
+    del g
     return {"value": round(aggregate_us_per_layer(e2e_ms, sz.n_layers, world), 4), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "accepted_last_step": int(out_host[0])}
 
 
 def run_ours(args):

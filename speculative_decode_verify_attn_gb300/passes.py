@@ -28,13 +28,14 @@ CHUNK = 64
 
 
 def _packed(layout, dev):
-    """One uint8 device buffer with 256-byte-aligned byte views {name: view} for [(name, nbytes)]."""
+    """One uint8 device buffer with 256-byte-aligned byte views {name: view} for [(name, nbytes)],
+    and the byte offset of every view."""
     offs, off = {}, 0
     for name, nbytes in layout:
         offs[name] = (off, nbytes)
         off += (nbytes + 255) // 256 * 256
     buf = torch.empty(off, dtype=torch.uint8, device=dev)
-    return buf, {name: buf.narrow(0, o, n) for name, (o, n) in offs.items()}
+    return buf, {name: buf.narrow(0, o, n) for name, (o, n) in offs.items()}, {k: o for k, (o, _) in offs.items()}
 
 
 def is_full_layer(layer: int) -> bool:
@@ -103,10 +104,13 @@ class VerifyPass:
         # One device buffer holds every per-step input (block queries, residency scores, logits,
         # drafts) and one holds every per-step result (accepted length, bonus, committed tokens),
         # so a caller moves a step's data with one copy each way.
+        # The order is the order a step needs them in: the residency scores (first kernel), the
+        # layers' queries, then the logits and drafts (last kernel).
         qbytes = self.n_layers * self.q * hq * d * 2
-        layout = [("q", qbytes), ("scores", self.n_chunks * 4), ("logits", self.q * workload.vocab * 4),
+        layout = [("scores", self.n_chunks * 4), ("q", qbytes), ("logits", self.q * workload.vocab * 4),
                   ("drafts", max(self.q - 1, 1) * 4)]
-        self.inputs, views = _packed(layout, dev)
+        self.inputs, views, self.input_offsets = _packed(layout, dev)
+        self.q_layer_bytes = self.q * hq * d * 2
         self.scores = views["scores"].view(torch.float32)
         self.scores.zero_()
         self.slot_of_chunk = torch.full((self.n_chunks,), -1, dtype=torch.int32, device=dev)
@@ -172,6 +176,7 @@ class VerifyPass:
         self.committed = self.results[2:]
         # Paging gets the higher priority: its CTAs go ahead of queued layer CTAs as SMs free up.
         self.side = torch.cuda.Stream(device=dev, priority=-1)
+        self.copy = torch.cuda.Stream(device=dev)       # host->device input copies (end to end)
         self.graph = None
         self.kernels_per_pass = None
         self.kernels_per_pass_append = None
@@ -248,10 +253,14 @@ class VerifyPass:
             vfy.vfy_append_swa(self.ctx, kn, vn, self.cu_q, self.seq_len, self.ring_offset, self.ring_k[l],
                                self.ring_v[l], 1, stream)
 
-    def enqueue(self, append: bool = False):
+    def enqueue(self, append: bool = False, waits: dict | None = None, paging_tail=None):
         """Enqueue one pass on the current stream (used for capture and for eager runs). With
         append, every layer first writes the block's own K/V rows (block KV append inside the
-        graph); without, they are a precondition of the pass."""
+        graph); without, they are a precondition of the pass. `waits` maps a layer index, or
+        "accept", to an event the chain waits for before that kernel (inputs still arriving).
+        `paging_tail`, if given, is called on the paging stream after the last page-in and
+        returns an event the acceptance waits for."""
+        waits = dict(waits or {})
         main = torch.cuda.current_stream(self.dev)
         events = {}
         joins = {}
@@ -272,9 +281,13 @@ class VerifyPass:
                     ev = torch.cuda.Event()
                     ev.record(self.side)
                     events[l] = ev
+                if paging_tail is not None:
+                    waits["accept"] = paging_tail()
             joins = join_points(len(self.full_layers))
         fi = 0
         for l in range(self.n_layers):
+            if l in waits:
+                main.wait_event(waits[l])
             if is_full_layer(l):
                 if fi in joins:
                     main.wait_event(events[self.full_layers[joins[fi]]])
@@ -286,10 +299,52 @@ class VerifyPass:
                 if append:
                     self.append_layer(l, main)
                 self.attend_swa_layer(l, main)
+        if "accept" in waits:
+            main.wait_event(waits["accept"])
         vfy.vfy_accept(self.ctx, self.logits, self.vocab, self.drafts, self.cu_rows, self.q, self.accepted,
                        self.bonus, self.committed, 1, main)
         if not self.all_resident:
             main.wait_stream(self.side)
+
+    def enqueue_end_to_end(self, in_host: torch.Tensor, out_host: torch.Tensor, front_layers: int = 4):
+        """One step from pinned host memory: copy the step's inputs (the image of self.inputs in
+        in_host) to the device, run the pass, and copy its results back to out_host. The scores
+        and the first `front_layers` layers' queries go first on the current stream; the other
+        queries follow on a copy stream while the first layers run. The logits and drafts, which
+        only the acceptance reads, go on the paging stream after the last page-in, so that they
+        do not share the host link with the page-ins. The chain waits for each part only where it
+        needs it."""
+        main = torch.cuda.current_stream(self.dev)
+        split_q = self.input_offsets["q"] + front_layers * self.q_layer_bytes
+        split_l = self.input_offsets["logits"]
+        n = self.inputs.numel()
+        self.inputs[:split_q].copy_(in_host[:split_q], non_blocking=True)
+        self.copy.wait_stream(main)
+        with torch.cuda.stream(self.copy):
+            self.inputs[split_q:split_l].copy_(in_host[split_q:split_l], non_blocking=True)
+            ev_q = torch.cuda.Event()
+            ev_q.record(self.copy)
+
+        def logits_after_paging():
+            self.inputs[split_l:n].copy_(in_host[split_l:n], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(torch.cuda.current_stream(self.dev))
+            return ev
+
+        self.enqueue(waits={front_layers: ev_q}, paging_tail=logits_after_paging)
+        out_host.copy_(self.results, non_blocking=True)
+
+    def capture_end_to_end(self, in_host: torch.Tensor, out_host: torch.Tensor):
+        """Capture enqueue_end_to_end as a graph (returned); the pass graph itself is unchanged."""
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                self.enqueue_end_to_end(in_host, out_host)
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        torch.cuda.synchronize(self.dev)
+        return graph
 
     def capture(self, append: bool = False):
         """Capture the pass as self.graph (with append, the variant that appends the block's

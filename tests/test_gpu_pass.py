@@ -144,3 +144,46 @@ def test_pass_with_block_kv_append(pass256k):
     assert_attn_close(bits(vp.outs[ls]), ref, f"window layer {ls} with append")
     assert_lse_close(vp.lses[ls].cpu().numpy(), rlse, f"window layer {ls} with append")
     assert vp.kernels_per_pass_append == vp.launches_per_step() + vp.n_layers
+
+
+def test_pass_end_to_end_from_host(pass256k):
+    """The end-to-end step (VerifyPass.enqueue_end_to_end, captured as one graph): the step's
+    inputs are copied from pinned host memory, the later layers' queries and the logits on a copy
+    stream while the first layers run, and the results come back to pinned host memory. With new
+    queries, logits and drafts placed only in the host image, one replay must leave the device
+    inputs equal to that image, produce the oracle's window-layer outputs for a layer whose
+    queries came with the first copy and for one whose queries came on the copy stream, and
+    return the oracle's acceptance on the new logits."""
+    vp = pass256k
+    hq, d = vp.shape.num_q_heads, vp.shape.head_dim
+    in_host = vp.inputs.cpu().pin_memory()
+    out_host = torch.full((vp.results.numel(),), -7, dtype=torch.int32).pin_memory()
+    g = vp.capture_end_to_end(in_host, out_host)
+    rng = np.random.default_rng(11)
+    gen = torch.Generator().manual_seed(12)
+    q_new = torch.randn((vp.n_layers, vp.q, hq, d), generator=gen).to(torch.bfloat16)
+    qo = vp.input_offsets["q"]
+    in_host[qo:qo + q_new.numel() * 2].copy_(q_new.reshape(-1).view(torch.uint8))
+    targets = rng.integers(0, vp.vocab, vp.q)
+    logits = synth.planted_logits(rng, targets, vp.vocab)
+    drafts = synth.drafts_matching(rng, targets, 0.5, vp.vocab).astype(np.int32)
+    lo, do = vp.input_offsets["logits"], vp.input_offsets["drafts"]
+    in_host[lo:lo + logits.nbytes].copy_(torch.from_numpy(logits.reshape(-1).view(np.uint8)))
+    in_host[do:do + drafts.nbytes].copy_(torch.from_numpy(drafts.view(np.uint8)))
+    so = vp.input_offsets["scores"]
+    sc = vp.score_table[vp.step % vp.score_table.shape[0]].cpu()
+    in_host[so:so + sc.numel() * 4].copy_(sc.view(torch.uint8))
+    vp.step += 1
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(vp.inputs.cpu(), in_host)
+    n, b, c = O.accept(logits, drafts, [0, vp.q])
+    got = out_host.numpy()
+    assert int(got[0]) == int(n[0]) and int(got[1]) == int(b[0])
+    assert got[2:].tolist() == c.tolist()
+    qbits = q_new.view(torch.int16).numpy().view(np.uint16)
+    for l in (vp.swa_layers[0], vp.swa_layers[5]):     # layer 0: first copy; layer 6: copy stream
+        ref, rlse = O.attend_ring_seq(qbits[l], bits(vp.ring_k[l])[0], bits(vp.ring_v[l])[0],
+                                      int(vp.ring_offset.item()), vp.L, synth.WINDOW)
+        assert_attn_close(bits(vp.outs[l]), ref, f"window layer {l} end to end")
+        assert_lse_close(vp.lses[l].cpu().numpy(), rlse, f"window layer {l} end to end")
