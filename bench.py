@@ -274,12 +274,12 @@ def oracle_steps(warm: int, steps: int, budget_s: float) -> dict:
     return {"warmup": warm, "steps": len(vals), "us_per_layer": vals, "timed_s": time.perf_counter() - t0}
 
 
-def run_oracle_child(budget_s: float, steps_spec: str = "") -> dict:
+def run_oracle_child(budget_s: float, steps_spec: str = "", threads: int = 1) -> dict:
     """Run the oracle sample (or the reference arm's loop, with steps_spec "W,K,budget") in a
-    child process pinned to one BLAS / OpenMP thread."""
+    child process whose BLAS / OpenMP pools have `threads` threads."""
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
-        env[var] = "1"
+        env[var] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__)]
     cmd += ["--oracle-steps", steps_spec] if steps_spec else ["--oracle-sample", str(budget_s)]
@@ -289,9 +289,10 @@ def run_oracle_child(budget_s: float, steps_spec: str = "") -> dict:
     return json.loads(out.stdout.strip().splitlines()[-1])
 
 
-def cpu_baseline_obj(res: dict) -> dict:
-    return {"value": round(res["us_per_layer"], 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"fp64 numpy oracle, one thread: 1 full layer (128 of 4096 chunks resident, 17 queries x "
+def cpu_baseline_obj(res: dict, cores: int = 1) -> dict:
+    threads = "one thread" if cores == 1 else f"{cores} BLAS threads"
+    return {"value": round(res["us_per_layer"], 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"fp64 numpy oracle, {threads}: 1 full layer (128 of 4096 chunks resident, 17 queries x "
                        f"16 heads), 1 window layer, residency top-128 of 4096, 16 page-ins, accept over 17 x 131072; "
                        f"{res['reps']} repetitions, scaled to 10 full + 30 window layers per pass / 40")}
 
@@ -690,6 +691,14 @@ def run_ours(args):
             cpu = cpu_baseline_obj(run_oracle_child(12.0))
         except Exception as e:  # reported, not fatal
             cpu = {"error": str(e)[:200]}
+        if not args.no_extras:
+            # the same sample with the BLAS pool on every host core (the oracle's matrix products
+            # run in parallel; its Python loops do not)
+            n_cores = os.cpu_count() or 1
+            try:
+                extras["cpu_baseline_all_cores"] = cpu_baseline_obj(run_oracle_child(8.0, threads=n_cores), n_cores)
+            except Exception as e:  # reported, not fatal
+                extras["cpu_baseline_all_cores"] = {"error": str(e)[:200]}
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -701,7 +710,9 @@ def run_ours(args):
                            "heads": "16q/4kv x 128", "l2": "flushed between steps (256 MiB write, then read back)",
                            "parallelism": f"replicas x{world}", "timing": "CUDA events around each graph replay"},
                 "kv_gbs": round(kv_gbs, 1), "kv_frac_of_hbm": round(kv_gbs / peak, 4),
-                "median_ms_per_step": round(med_ms, 5), "wall_s": round(wall, 3),
+                "median_ms_per_step": round(med_ms, 5),
+                "p90_ms_per_step": round(sorted(ts)[min(len(ts) - 1, (9 * len(ts)) // 10)], 5),
+                "wall_s": round(wall, 3),
                 "pass_bytes": sz.bytes_pass, "accepted_last_step": accepted,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
                 "e2e": e2e,
