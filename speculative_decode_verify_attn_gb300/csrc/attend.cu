@@ -160,21 +160,23 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
     w.nres = max(0, p.cu_res[w.b + 1] - w.r0);
     n_tiles = (w.nres + CPT - 1) / CPT;
   } else {
+    // Unsigned 32-bit arithmetic on the way to the first load: lo < 2^31 and phi < R <= 2^31, so
+    // lo + phi fits.
     const int R = p.ring_len;
-    int phi = p.ring_off[w.b];
-    phi = ((phi % R) + R) % R;
+    const unsigned phi = static_cast<unsigned>(p.ring_off[w.b] % R + R) % static_cast<unsigned>(R);
     // The tile's queries are i in [row0 / G, (row0 + rows - 1) / G], at positions L - nq + i.
     const bool whole = p.row_tiles == 1;               // then the tile is the whole block
     const int i_first = whole ? 0 : w.row0 / p.group;
     const int i_last = whole ? w.nq - 1 : (w.row0 + w.rows - 1) / p.group;
     w.lo = max(0, w.L - w.nq + i_first - p.window + 1);
     w.span = w.L - w.nq + i_last + 1 - w.lo;
-    w.s_lo = static_cast<int>((static_cast<long long>(w.lo) + phi) % R);
+    w.s_lo = static_cast<int>((static_cast<unsigned>(w.lo) + phi) % static_cast<unsigned>(R));
     n_tiles = w.span > 0 ? ((w.s_lo & (kChunk - 1)) + w.span + kChunk - 1) / kChunk : 0;
   }
-  const long long ns = p.num_splits;
-  w.tb = static_cast<int>((static_cast<long long>(w.s) * n_tiles) / ns);
-  w.nt = static_cast<int>((static_cast<long long>(w.s + 1) * n_tiles) / ns) - w.tb;
+  // (s + 1) * n_tiles < 64 * 2^26: unsigned 32-bit division
+  const unsigned ns = static_cast<unsigned>(p.num_splits);
+  w.tb = static_cast<int>((static_cast<unsigned>(w.s) * static_cast<unsigned>(n_tiles)) / ns);
+  w.nt = static_cast<int>((static_cast<unsigned>(w.s + 1) * static_cast<unsigned>(n_tiles)) / ns) - w.tb;
   return w;
 }
 
@@ -202,11 +204,12 @@ __device__ __forceinline__ Tile tile_at(const AttnParams& p, const Work& w, int 
     t.base = t.valid ? cid * kChunk : 0;
   } else {
     const int R = p.ring_len;
-    const int tiles_per_ring = R / kChunk;
-    const int ti = (w.s_lo / kChunk + w.tb + j) % tiles_per_ring;
+    const unsigned tiles_per_ring = static_cast<unsigned>(R / kChunk);
+    const int ti = static_cast<int>(static_cast<unsigned>(w.s_lo / kChunk + w.tb + j) % tiles_per_ring);
     t.valid = true;
     t.y = ((w.b * p.hkv + w.h) * R) + ti * kChunk;
-    t.base = ((ti * kChunk - w.s_lo) % R + R) % R;
+    const int d = ti * kChunk - w.s_lo;                // in (-R, R)
+    t.base = d < 0 ? d + R : d;
   }
   return t;
 }
