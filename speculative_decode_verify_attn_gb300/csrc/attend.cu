@@ -510,8 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool active = __any_sync(0xffffffffu, lr < w.rows);  // the warp holds a row of the block
     const bool rv = lr < w.rows;
     const int r = w.row0 + lr;                         // block row: query r / G, q-head r % G
-    const int qi = rv ? r / p.group : 0;
-    const int g = rv ? r % p.group : 0;
+    const unsigned ug = static_cast<unsigned>(p.group);   // unsigned division: fewer instructions
+    const int qi = rv ? static_cast<int>(static_cast<unsigned>(r) / ug) : 0;
+    const int g = rv ? static_cast<int>(static_cast<unsigned>(r) % ug) : 0;
     // Q row -> swizzled smem (the 128-byte swizzle TMA would apply: chunk c of row m at c ^ (m & 7)).
     // Each warpgroup stages half of the row's 16-byte chunks.
     {
@@ -715,8 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t recv_ml = smem_u32(smem + C::kRecvMlOffset);
       for (int rr = warp; rr < w.rows; rr += kSoftmaxThreads / 32) {
         const float2 ml = bars->sml[rr];
-        const int e = (rr / n) * n + rank;             // entry in the owner's receive area
-        const uint32_t owner = static_cast<uint32_t>(rr % n);
+        const unsigned rq = static_cast<unsigned>(rr) / static_cast<unsigned>(n);
+        const int e = static_cast<int>(rq) * n + rank;  // entry in the owner's receive area
+        const uint32_t owner = static_cast<uint32_t>(rr - static_cast<int>(rq) * n);
         if (lane == 0) st_dsmem_f2(dsmem_addr(recv_ml + e * 8, owner), ml);
         if (ml.y > 0.f) {
           const uint32_t dst = dsmem_addr(recv + (e * HD + lane * kPer) * 4, owner);
@@ -800,8 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const int t = w.q0 + (w.row0 + r) / p.group;      // r is the row within this tile
-      const int hq = w.h * p.group + (w.row0 + r) % p.group;
+      const unsigned br = static_cast<unsigned>(w.row0 + r);   // r is the row within this tile
+      const unsigned bq = br / static_cast<unsigned>(p.group);
+      const int t = w.q0 + static_cast<int>(bq);
+      const int hq = w.h * p.group + static_cast<int>(br - bq * static_cast<unsigned>(p.group));
       if (t < p.token_cap) {
         uint16_t* dst = p.out + (static_cast<size_t>(t) * p.hq + hq) * HD + lane * kPer;
         if constexpr (kPer == 4) {
@@ -857,8 +861,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int i = t - p.cu_q[b];
   const int nq = p.cu_q[b + 1] - p.cu_q[b];
   if (i < 0 || nq < 0 || nq > p.max_q || p.seq_len[b] < nq) return;   // skipped by the attention kernel too
-  const int h = hq / p.group;
-  const int rg = i * p.group + hq % p.group;              // block row
+  const int h = static_cast<int>(static_cast<unsigned>(hq) / static_cast<unsigned>(p.group));
+  const int rg = i * p.group + (hq - h * p.group);        // block row
   const int rt = rg / kMaxRows;                           // its row tile
   const int r = rg - rt * kMaxRows;                       // and its row within the tile
   const size_t p0 = ((static_cast<size_t>(b) * p.row_tiles + rt) * p.hkv + h) * p.num_splits;

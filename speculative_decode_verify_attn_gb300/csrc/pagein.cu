@@ -21,7 +21,7 @@ constexpr int kUnroll = 2;
 __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p) {
   pdl_wait();
   const int e = blockIdx.x;
-  const int b = e / p.k;
+  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.k));
   const int i = e - b * p.k;
   if (b >= p.num_seqs || i >= p.count[b]) return;
   const int chunk = p.list[2 * e];
