@@ -136,9 +136,15 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
   w.row0 = w.rt * kMaxRows;
   w.h = blockIdx.y;
   w.s = blockIdx.x;
-  w.q0 = p.cu_q[w.b];
-  w.nq = p.cu_q[w.b + 1] - w.q0;
-  w.L = p.seq_len[w.b];
+  // Every per-sequence value is loaded at once (one round trip to memory before the first tile
+  // can be addressed); all of them are in bounds for every b < B.
+  const int cq0 = p.cu_q[w.b], cq1 = p.cu_q[w.b + 1], len = p.seq_len[w.b];
+  const int cr0 = RING ? 0 : p.cu_res[w.b];
+  const int cr1 = RING ? 0 : p.cu_res[w.b + 1];
+  const int roff = RING ? p.ring_off[w.b] : 0;
+  w.q0 = cq0;
+  w.nq = cq1 - cq0;
+  w.L = len;
   w.tb = 0;
   w.nt = 0;
   w.r0 = 0;
@@ -156,14 +162,14 @@ __device__ __forceinline__ Work make_work(const AttnParams& p) {
   if (w.rows == 0) return w;                     // a row tile past this sequence's block
   int n_tiles;
   if (!RING) {
-    w.r0 = p.cu_res[w.b];
-    w.nres = max(0, p.cu_res[w.b + 1] - w.r0);
+    w.r0 = cr0;
+    w.nres = max(0, cr1 - cr0);
     n_tiles = (w.nres + CPT - 1) / CPT;
   } else {
     // Unsigned 32-bit arithmetic on the way to the first load: lo < 2^31 and phi < R <= 2^31, so
     // lo + phi fits.
     const int R = p.ring_len;
-    const unsigned phi = static_cast<unsigned>(p.ring_off[w.b] % R + R) % static_cast<unsigned>(R);
+    const unsigned phi = static_cast<unsigned>(roff % R + R) % static_cast<unsigned>(R);
     // The tile's queries are i in [row0 / G, (row0 + rows - 1) / G], at positions L - nq + i.
     const bool whole = p.row_tiles == 1;               // then the tile is the whole block
     const int i_first = whole ? 0 : w.row0 / p.group;
