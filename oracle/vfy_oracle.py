@@ -20,7 +20,7 @@ What it restates, and where the pages say so (cited by page title and section):
 [WD] "Width vs. Depth: Speculating on the Margin": ragged speculation, a draft depth per
      sequence.
 
-Readings taken where the pages are silent (each is also listed in the design doc):
+Readings taken where the pages are silent:
   * L (the sequence length) counts the verify block itself; query i of a q-token block sits at
     position L - q + i.
   * Residency is top-k over fp32 scores: higher score first, ties to the lower chunk index,
