@@ -859,14 +859,21 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = static_cast<int>(blockIdx.x / p.hq);
   const int hq = static_cast<int>(blockIdx.x % p.hq);
-  if (t >= p.token_cap) return;
+  // One round trip for a one-sequence batch: its values are loaded with the batch's token count
+  // (all in bounds: cu_q has B + 1 entries, seq_len B). A batch searches for its sequence.
   const int total = p.cu_q[p.num_seqs];
-  if (t >= total) return;
   int b = 0;
-  while (b + 1 < p.num_seqs && p.cu_q[b + 1] <= t) ++b;
-  const int i = t - p.cu_q[b];
-  const int nq = p.cu_q[b + 1] - p.cu_q[b];
-  if (i < 0 || nq < 0 || nq > p.max_q || p.seq_len[b] < nq) return;   // skipped by the attention kernel too
+  int c0 = p.cu_q[0], c1 = p.cu_q[1], len = p.seq_len[0];
+  if (t >= p.token_cap || t >= total) return;
+  if (p.num_seqs > 1) {
+    while (b + 1 < p.num_seqs && p.cu_q[b + 1] <= t) ++b;
+    c0 = p.cu_q[b];
+    c1 = p.cu_q[b + 1];
+    len = p.seq_len[b];
+  }
+  const int i = t - c0;
+  const int nq = c1 - c0;
+  if (i < 0 || nq < 0 || nq > p.max_q || len < nq) return;   // skipped by the attention kernel too
   const int h = static_cast<int>(static_cast<unsigned>(hq) / static_cast<unsigned>(p.group));
   const int rg = i * p.group + (hq - h * p.group);        // block row
   const int rt = rg / kMaxRows;                           // its row tile
