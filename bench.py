@@ -15,7 +15,11 @@ One JSON line on stdout (rank 0):
                 holds none of its inputs and no dirty lines
   e2e           the same, with the step's inputs copied host->device from pinned memory and the
                 accepted tokens copied back inside the timed region
-  roofline      for the dominant kernel (full-layer attention): algorithmic bytes / event time
+  kernels       per kernel of the pass (window attention, full attention + combine, acceptance):
+                launches per pass, device time per launch in a chain of its own launches (CUDA
+                events around one graph replay of that chain, L2 flushed before it), algorithmic
+                bytes per launch, GB/s, fraction of HBM, share of the pass
+  roofline      the kernels entry with the largest share of the pass
   cpu_baseline  the fp64 CPU oracle on a bounded sample, one host core
 Multi-GPU (torchrun): replicas only, one pass per GPU, no collective on the data path.
 """
@@ -260,23 +264,9 @@ def oracle_sample_seconds(budget_s: float) -> dict:
     return {"us_per_layer": pass_s * 1e6 / 40, "reps": reps, "parts_s": m, "pass_s": pass_s}
 
 
-def oracle_steps(warm: int, steps: int, budget_s: float) -> dict:
-    """The reference arm's loop, in one process: `warm` untimed repetitions, then up to `steps`
-    timed ones, stopping early once budget_s of timed work has run (at least one step). Each
-    step is one repetition scaled to the pass; returns every step's us per layer."""
-    rep = _oracle_rep_fn()
-    for _ in range(warm):
-        rep()
-    vals = []
-    t0 = time.perf_counter()
-    while len(vals) < steps and (not vals or time.perf_counter() - t0 < budget_s):
-        vals.append(_pass_seconds(rep()) * 1e6 / 40)
-    return {"warmup": warm, "steps": len(vals), "us_per_layer": vals, "timed_s": time.perf_counter() - t0}
-
-
 def run_oracle_child(budget_s: float, steps_spec: str = "", threads: int = 1) -> dict:
-    """Run the oracle sample (or the reference arm's loop, with steps_spec "W,K,budget") in a
-    child process whose BLAS / OpenMP pools have `threads` threads."""
+    """Run the oracle sample (or the reference arm's whole-pass loop, with steps_spec
+    "W,K,budget") in a child process whose BLAS / OpenMP pools have `threads` threads."""
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[var] = str(threads)
@@ -302,7 +292,70 @@ def cpu_baseline_obj(res: dict, cores: int = 1) -> dict:
 # ---------------------------------------------------------------------------------------------
 
 REFERENCE_WARMUP = (3, 5)       # the reference arm's warm-up steps: at least 3, at most 5
-REFERENCE_BUDGET_S = 120.0      # timed oracle work at most (about 1.3 s a step on one core)
+REFERENCE_BUDGET_S = 120.0      # timed oracle work at most (a whole pass takes seconds on one core)
+
+
+def _oracle_pass_fn():
+    """Build the inputs of the whole 40-layer pass once and return a function that runs one step
+    of it through the oracle: residency top-128 of 4096 chunks (16 new chunks per step), the 16
+    page-ins of each of the 10 full layers, the 10 full layers over their 8K-token pools, the 30
+    window layers over their rings (window 512, ring 2048, wrapping) and the acceptance over
+    17 x 131072 logits. The host store of each full layer holds 32 distinct chunks, which stand
+    for the 4096 of the context (a page-in copies chunk id mod 32: the same bytes moved)."""
+    import numpy as np
+
+    from oracle import vfy_oracle as O
+    from speculative_decode_verify_attn_gb300 import synth
+
+    rng = np.random.default_rng(0)
+    s = synth.LAGUNA
+    L, q, n, k = 262144, 17, 4096, 128
+    layers = list(range(40))
+    full = [l for l in layers if l % 4 == 3]
+    swa = [l for l in layers if l % 4 != 3]
+    rot = synth.rotating_residency(rng, n, k, 16, L, q)
+    hkv, d = s.num_kv_heads, s.head_dim
+    pools = {l: [synth.normal_bf16(rng, (k, hkv, 64, d)), synth.normal_bf16(rng, (k, hkv, 64, d))] for l in full}
+    stores = {l: (synth.normal_bf16(rng, (32, hkv, 64, d)), synth.normal_bf16(rng, (32, hkv, 64, d))) for l in full}
+    rings = {l: (synth.normal_bf16(rng, (hkv, synth.RING, d)), synth.normal_bf16(rng, (hkv, synth.RING, d)))
+             for l in swa}
+    phi = synth.wrapping_ring_offset(rng, L, synth.WINDOW + q - 1, synth.RING)
+    qs = {l: synth.normal_bf16(rng, (q, s.num_q_heads, d)) for l in layers}
+    targets = rng.integers(0, synth.VOCAB, q)
+    logits = synth.planted_logits(rng, targets, synth.VOCAB)
+    drafts = synth.drafts_matching(rng, targets, 0.56, synth.VOCAB)
+    state = {"soc": np.full(n, -1), "t": 0}
+
+    def step() -> float:
+        t0 = time.perf_counter()
+        res = O.select_resident(rot.scores(state["t"]), [0, n], k, state["soc"])
+        state["soc"], state["t"] = res["slot_of_chunk"], state["t"] + 1
+        pairs = [(c % 32, s_) for c, s_ in res["pagein"][0]]
+        for l in full:
+            pools[l] = list(O.page_in(stores[l][0], stores[l][1], pools[l][0], pools[l][1], pairs))
+        for l in layers:
+            if l in pools:
+                O.attend_full_seq(qs[l], pools[l][0], pools[l][1], res["resident_ids"], res["resident_slots"], L)
+            else:
+                O.attend_ring_seq(qs[l], rings[l][0], rings[l][1], phi, L, synth.WINDOW)
+        O.accept(logits, drafts, [0, q])
+        return time.perf_counter() - t0
+
+    return step
+
+
+def oracle_pass_steps(warm: int, steps: int, budget_s: float) -> dict:
+    """The reference arm's loop, in one process: `warm` untimed whole-pass steps, then up to
+    `steps` timed ones, stopping early once budget_s of timed work has run (at least one step).
+    Returns every timed step's seconds."""
+    step = _oracle_pass_fn()
+    for _ in range(warm):
+        step()
+    secs = []
+    t0 = time.perf_counter()
+    while len(secs) < steps and (not secs or time.perf_counter() - t0 < budget_s):
+        secs.append(step())
+    return {"warmup": warm, "steps": len(secs), "step_s": secs, "timed_s": time.perf_counter() - t0}
 
 
 def run_reference(args):
@@ -314,19 +367,21 @@ def run_reference(args):
     t0 = time.perf_counter()
     res = run_oracle_child(0.0, f"{warm},{steps},{REFERENCE_BUDGET_S}")
     wall = time.perf_counter() - t0
-    vals = res["us_per_layer"]
-    value = statistics.mean(vals)
-    sample = (f"fp64 numpy oracle, one thread; each step: 1 full layer (128 of 4096 chunks resident, 17 queries "
-              f"x 16 heads), 1 window layer, residency top-128 of 4096, 16 page-ins, accept over 17 x 131072, "
-              f"scaled to 10 full + 30 window layers per pass / 40")
+    secs = res["step_s"]
+    ms_per_step = 1000.0 * statistics.mean(secs)
+    value = ms_per_step * 1000.0 / 40
+    sample = ("fp64 numpy oracle, one thread; each step is the whole 40-layer pass: residency top-128 of 4096, "
+              "16 page-ins into each of 10 pools, 10 full layers (128 of 4096 chunks resident, 17 queries x 16 heads), "
+              "30 window layers, accept over 17 x 131072")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
             "n_gpus": args.gpus, "steps": res["steps"], "warmup": res["warmup"],
-            "ms_per_step": round(value * 40 / 1000, 3),
+            "ms_per_step": round(ms_per_step, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": "verify pass, 256K context, 16-token draft (sampled on the CPU)",
+            "config": {"workload": "verify pass, 256K context, 16-token draft, 10 full (8K pool) + 30 window layers "
+                                   "(fp64 oracle on the host cores, whole pass per step)",
                        "steps_requested": args.steps, "timed_budget_s": REFERENCE_BUDGET_S,
-                       "wall_s": round(wall, 2)},
+                       "timed_s": round(res["timed_s"], 2), "wall_s": round(wall, 2)},
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -355,25 +410,85 @@ def event_time_graph(graph, flush, steps, pre=None):
     return statistics.mean(ts), statistics.median(ts), ts
 
 
-PROFILE_8K = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "attend_full_8k_resident.md")
-ATTEND_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "speculative_decode_verify_attn_gb300",
-                          "csrc", "attend.cu")
+PROFILES = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
+CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "speculative_decode_verify_attn_gb300", "csrc")
+NOMINAL_HBM_GBS = 7900.0        # GB300 HBM3e, nominal (context beside the measured peak)
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the full-layer attention kernel from its committed ncu summary,
-    or None when the kernel source differs from the one the counters were taken on."""
+def profiled_traffic(profile: str, source: str):
+    """DRAM bytes per launch of a kernel from its committed ncu summary (profiles/<profile>, the
+    lines "traffic_bytes: N" and "source_sha256_16: H"), or None when csrc/<source> differs from
+    the source the counters were taken on."""
     import hashlib
     try:
-        text = open(PROFILE_8K).read()
+        text = open(os.path.join(PROFILES, profile)).read()
         fields = dict(line.split(": ", 1) for line in text.splitlines()
                       if line.startswith(("traffic_bytes: ", "source_sha256_16: ")))
-        src = hashlib.sha256(open(ATTEND_SRC, "rb").read()).hexdigest()[:16]
+        src = hashlib.sha256(open(os.path.join(CSRC, source), "rb").read()).hexdigest()[:16]
         if fields.get("source_sha256_16", "").strip() != src:
             return None
         return int(fields["traffic_bytes"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def chain_points(vp, flush, steps, peak, peak_kind):
+    """Per-kernel device time in a chain of the kernel's own launches, as the pass runs them
+    (programmatic dependent launch between neighbours, one CUDA graph): the pass's 30 window
+    layers alone, its 10 full layers alone (attention + combine each), and 8 acceptances over 8
+    distinct 17 x 131072 logit buffers (71 MB, so each reads HBM after the flush). CUDA events
+    around each replay on the replaying stream, L2 flushed before it; time per launch = replay
+    time / launches. Each entry: algorithmic bytes per launch, GB/s, fraction of the HBM peak,
+    and its share of the pass (launches per pass x time per launch over the sum)."""
+    import torch
+
+    from speculative_decode_verify_attn_gb300 import vfy
+    sz = vp.sizes()
+
+    def swa_chain():
+        for l in vp.swa_layers:
+            vp.attend_swa_layer(l)
+
+    def full_chain():
+        for l in vp.full_layers:
+            vp.attend_full_layer(l)
+
+    n_acc = 8
+    logit_bufs = [vp.logits.clone() for _ in range(n_acc)]
+
+    def accept_chain():
+        for lg in logit_bufs:
+            vfy.vfy_accept(vp.ctx, lg, vp.vocab, vp.drafts, vp.cu_rows, vp.q, vp.accepted, vp.bonus, vp.committed, 1)
+
+    n0 = vfy.vfy_launch_count(vp.ctx)
+    g_full = capture(full_chain)
+    full_kernels = (vfy.vfy_launch_count(vp.ctx) - n0) // 2 // len(vp.full_layers)   # eager run + capture
+    out = {}
+    for name, fn, launches, per_pass, nbytes, kernel, profile in (
+            ("window_attention", swa_chain, len(vp.swa_layers), len(vp.swa_layers), sz.bytes_swa,
+             "attend_kernel<128,true,true,false> (window 512 in a 2048-slot ring, splits merged in a cluster)",
+             "attend_swa_window512.md"),
+            ("full_attention", None, len(vp.full_layers), len(vp.full_layers), sz.bytes_full,
+             f"attend_kernel<128,false,...> + its split merge (8K resident of 256K; {full_kernels} kernel(s) a layer)",
+             "attend_full_8k_resident.md"),
+            ("accept", accept_chain, n_acc, 1, sz.bytes_accept,
+             "accept_kernel<true> (argmax + greedy acceptance, 17 x 131072 fp32)", "accept_17x131072.md")):
+        g = g_full if fn is None else capture(fn)
+        mean_ms, med_ms, _ = event_time_graph(g, flush, steps)
+        del g
+        us = mean_ms * 1000.0 / launches
+        gbs = nbytes / (us * 1e-6) / 1e9
+        src = "accept.cu" if name == "accept" else "attend.cu"
+        out[name] = {"kernel": kernel, "launches_per_pass": per_pass, "us_per_launch": round(us, 3),
+                     "chain_launches": launches, "algorithmic_bytes": nbytes, "achieved": round(gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                     "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "peak_kind": peak_kind,
+                     "traffic": profiled_traffic(profile, src)}
+    del g_full, logit_bufs
+    total = sum(e["us_per_launch"] * e["launches_per_pass"] for e in out.values())
+    for e in out.values():
+        e["pass_share"] = round(e["us_per_launch"] * e["launches_per_pass"] / total, 4)
+    return out
 
 
 def prefill_shaped_point(vp, flush, local, rank, steps, tf_peak):
@@ -628,11 +743,16 @@ def run_ours(args):
         k_steps = max(50, min(args.steps, 500))
         f_mean, f_med, _ = event_time_graph(g_full, flush, k_steps)
         s_mean, s_med, _ = event_time_graph(g_swa, flush, k_steps)
-        achieved = sz.bytes_full / (f_mean * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "attend_kernel<128,false> + combine (one full layer, 8K resident)",
-                    "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
-                    "algorithmic_bytes": sz.bytes_full, "peak_kind": peak_kind}
+        # per kernel, in a chain of its own launches; the roofline is the one with the largest
+        # share of the pass
+        kernels = chain_points(vp, flush, k_steps, peak, peak_kind)
+        extras["kernels"] = kernels
+        top = max(kernels, key=lambda name: kernels[name]["pass_share"])
+        e = kernels[top]
+        roofline = {"bound": "hbm", "kernel": f"{top}: {e['kernel']}", "achieved": e["achieved"], "peak": peak,
+                    "unit": "GB/s", "frac": e["frac"], "traffic": e["traffic"],
+                    "algorithmic_bytes": e["algorithmic_bytes"], "us_per_launch": e["us_per_launch"],
+                    "pass_share": e["pass_share"], "peak_kind": peak_kind}
         g_layers = capture(vp.enqueue_layers)
         l_mean, _, _ = event_time_graph(g_layers, flush, k_steps)
         g_acc = capture(vp.enqueue_accept)
@@ -654,6 +774,7 @@ def run_ours(args):
         extras["select_plus_pagein_us"] = round(p_mean * 1000, 3)
         extras["pagein_host_gbs"] = round(pg_bytes / (p_mean * 1e-3) / 1e9, 1)
         del g_layers, g_acc, g_pg
+        # one layer alone in a graph of its own (includes the graph's launch)
         extras["full_layer_us"] = round(f_mean * 1000, 3)
         extras["swa_layer_us"] = round(s_mean * 1000, 3)
         extras["swa_layer_gbs"] = round(sz.bytes_swa / (s_mean * 1e-3) / 1e9, 1)
@@ -666,7 +787,9 @@ def run_ours(args):
         a_bytes = ar.sizes().bytes_full
         extras["all_resident_256k_layer"] = {"us": round(a_mean * 1000, 2), "bytes": a_bytes,
                                              "gbs": round(a_bytes / (a_mean * 1e-3) / 1e9, 1),
-                                             "frac": round(a_bytes / (a_mean * 1e-3) / 1e9 / peak, 4)}
+                                             "frac": round(a_bytes / (a_mean * 1e-3) / 1e9 / peak, 4),
+                                             "frac_of_nominal": round(a_bytes / (a_mean * 1e-3) / 1e9 /
+                                                                      NOMINAL_HBM_GBS, 4)}
         # the same two graphs with the write-only flush: the L2 starts each step full of dirty lines
         dflush = flush.dirty()
         d_ar, _, _ = event_time_graph(g_ar, dflush, max(20, min(args.steps, 200)))
@@ -691,14 +814,6 @@ def run_ours(args):
             cpu = cpu_baseline_obj(run_oracle_child(12.0))
         except Exception as e:  # reported, not fatal
             cpu = {"error": str(e)[:200]}
-        if not args.no_extras:
-            # the same sample with the BLAS pool on every host core (the oracle's matrix products
-            # run in parallel; its Python loops do not)
-            n_cores = os.cpu_count() or 1
-            try:
-                extras["cpu_baseline_all_cores"] = cpu_baseline_obj(run_oracle_child(8.0, threads=n_cores), n_cores)
-            except Exception as e:  # reported, not fatal
-                extras["cpu_baseline_all_cores"] = {"error": str(e)[:200]}
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -710,6 +825,7 @@ def run_ours(args):
                            "heads": "16q/4kv x 128", "l2": "flushed between steps (256 MiB write, then read back)",
                            "parallelism": f"replicas x{world}", "timing": "CUDA events around each graph replay"},
                 "kv_gbs": round(kv_gbs, 1), "kv_frac_of_hbm": round(kv_gbs / peak, 4),
+                "kv_frac_of_nominal_hbm": round(kv_gbs / NOMINAL_HBM_GBS, 4),
                 "median_ms_per_step": round(med_ms, 5),
                 "p90_ms_per_step": round(sorted(ts)[min(len(ts) - 1, (9 * len(ts)) // 10)], 5),
                 "wall_s": round(wall, 3),
@@ -727,7 +843,7 @@ def main(argv=None):
     args = parse_args(argv)
     if args.oracle_steps:
         w, k, budget = args.oracle_steps.split(",")
-        print(json.dumps(oracle_steps(int(w), int(k), float(budget))))
+        print(json.dumps(oracle_pass_steps(int(w), int(k), float(budget))))
         return 0
     if args.oracle_sample or "--oracle-sample" in (argv or sys.argv):
         print(json.dumps(oracle_sample_seconds(args.oracle_sample)))

@@ -109,6 +109,15 @@ VFY_API unsigned long long vfy_launch_count(const vfy_ctx* ctx);
  * through the combine kernel. */
 VFY_API vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits);
 
+/* Set the time limit of the attention kernels' pipeline waits (each wait for a copy, an MMA or
+ * another warp's step), in nanoseconds; 0 restores the default of 2 s. Diagnostic and test knob:
+ * a wait that runs out sets VFY_EDEVICE_TIMEOUT in the device error word, the kernel lets the
+ * copies and MMAs it issued land (with the default limit), frees its tensor memory and returns;
+ * that call's outputs are then undefined. The context stays usable: vfy_get_status reports and
+ * clears the error, and later calls produce correct results. A limit of a few nanoseconds makes
+ * the first wait that is not already complete run out. Applies to calls enqueued afterwards. */
+VFY_API vfy_status vfy_set_wait_limit(vfy_ctx* ctx, uint64_t limit_ns);
+
 /*
  * vfy_select_resident -- chunk-residency top-k and slot reconciliation.
  * Source: "Laguna XS 2.1 33B on a RTX 3090" (lucebox), "Three optimizations", item 1: the pool
@@ -300,9 +309,14 @@ VFY_API vfy_status vfy_accept(vfy_ctx* ctx, const float* logits, int vocab, cons
  * it), with max_rows (a host bound on cu_rows[B]) at most 1024: a larger max_rows returns
  * VFY_EINVAL and launches nothing. device_error (nullable) is a caller-owned device int32 that
  * receives VFY device error bits (1 = out-of-range list, 2 = timeout) OR-ed in; the caller clears it.
+ * With device_error NULL, device errors go to a word inside the scratch array that the next
+ * call clears and no call reads: they are discarded, and the outputs of a call that hit one are
+ * unspecified. Pass a word to see them.
  *  - The first call on a device looks up the scratch array's device address
  *    (cudaGetSymbolAddress) with that device current. Make that first call before any stream
- *    capture.
+ *    capture. The address is cached per device; a call that finds another context current on
+ *    the device (after cudaDeviceReset, say) looks it up again, so make the first call after a
+ *    reset outside capture too. Device ordinals of 64 and above return VFY_EUNSUPPORTED.
  *  - Each call clears the scratch on `stream` (cudaMemsetAsync) and then launches the kernel; it
  *    calls no cudaMalloc, cudaFree or other allocating routine.
  *  - Every call on a device shares the one array: calls whose work overlaps on the GPU (other

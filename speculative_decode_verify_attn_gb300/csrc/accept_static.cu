@@ -22,24 +22,48 @@ static __device__ __align__(256) unsigned long long g_accept_scratch[kStaticMaxR
 
 struct DeviceState {
   unsigned long long* scratch = nullptr;   // device address of g_accept_scratch on this device
+  CUcontext ctx = nullptr;                 // the context that address belongs to
   int num_sms = 0;
 };
 std::mutex g_lock;
 DeviceState g_state[kMaxDevices];
 
-// Once per device, with that device current: look up the device address of the scratch array.
-// (In host code, g_accept_scratch names a host-side stand-in, not device memory.)
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The driver's current context, through the runtime's entry-point query (no link to libcuda).
+bool current_context(CUcontext* out) {
+  static CtxGetCurrentFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  return fn(out) == CUDA_SUCCESS;
+}
+
+// With the device current: look up the device address of the scratch array. (In host code,
+// g_accept_scratch names a host-side stand-in, not device memory.) The address is cached per
+// device and looked up again when the device's context has changed (after cudaDeviceReset the
+// old address is gone).
 cudaError_t device_state(int dev, DeviceState* out) {
   std::lock_guard<std::mutex> guard(g_lock);
   DeviceState& st = g_state[dev];
-  if (st.scratch == nullptr) {
+  CUcontext cur = nullptr;
+  if (!current_context(&cur)) return cudaErrorUnknown;
+  if (st.scratch == nullptr || st.ctx != cur) {
     void* ptr = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_accept_scratch);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    // cudaGetSymbolAddress made the device's primary context current if none was
+    if (!current_context(&cur)) return cudaErrorUnknown;
     st.scratch = static_cast<unsigned long long*>(ptr);
+    st.ctx = cur;
     st.num_sms = sms;
   }
   *out = st;
@@ -61,10 +85,11 @@ extern "C" vfy_status vfy_accept_static(const float* logits, int vocab, const in
   if (max_rows > kStaticMaxRows) return VFY_EINVAL;   // beyond the fixed scratch: refused
   if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0) return VFY_EINVAL;
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     (void)cudaGetLastError();
     return VFY_ECUDA;
   }
+  if (dev >= kMaxDevices) return VFY_EUNSUPPORTED;   // beyond the per-device address cache
   DeviceState st;
   if (device_state(dev, &st) != cudaSuccess) {
     (void)cudaGetLastError();

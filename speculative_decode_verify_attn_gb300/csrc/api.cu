@@ -27,6 +27,7 @@ struct vfy_ctx {
   int swa_splits;
   unsigned long long launches;   // kernels enqueued through this context
   int row_tiles;                 // ceil(max_queries_per_seq * G / 128)
+  unsigned long long wait_limit_ns;   // attention pipeline waits (0 = the default)
 };
 
 namespace {
@@ -216,6 +217,12 @@ vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits) {
   VFY_REQUIRE(swa_splits >= 0 && swa_splits <= ctx->cfg.max_splits);
   ctx->full_splits = full_splits;
   ctx->swa_splits = swa_splits;
+  return VFY_OK;
+}
+
+vfy_status vfy_set_wait_limit(vfy_ctx* ctx, uint64_t limit_ns) {
+  VFY_REQUIRE(ctx != nullptr);
+  ctx->wait_limit_ns = limit_ns;
   return VFY_OK;
 }
 
@@ -430,6 +437,7 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   p.scale_log2 = ctx->scale * 1.4426950408889634f;
   p.part_o = ctx->part_o;
   p.part_ml = ctx->part_ml;
+  p.wait_limit_ns = ctx->wait_limit_ns;
   p.err = ctx->err;
   // Full-layer splits over many resident chunks take wide tiles (their combine is a small part
   // of a long split). Otherwise up to kMaxClusterSplits splits (and no more than one GPC holds)

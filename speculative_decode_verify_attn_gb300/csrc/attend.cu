@@ -327,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort = &bars->abort;
+  const WaitLimit wl = make_wait_limit(p.wait_limit_ns);
 
   // Let the next kernel in the stream launch now: its prologue overlaps this kernel, and its
   // griddepcontrol.wait still waits for this grid to complete.
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool reported = false;
       for (int j = 0; j < w.nt; ++j) {
         const int st = j % C::kKStages;
-        if (j >= C::kKStages && !mbar_wait(&bars->k_empty[st], ((j / C::kKStages) - 1) & 1, abort, p.err)) break;
+        if (j >= C::kKStages && !mbar_wait(&bars->k_empty[st], ((j / C::kKStages) - 1) & 1, abort, p.err, wl)) break;
         Tile t[C::kCPT];
         int n_present = 0;
         bool zero = false;
@@ -398,11 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = j + 1;
       }
-      if (*abort) {
-        // Let every copy still in flight land before the CTA can exit.
-        for (int j = max(0, issued - C::kKStages); j < issued; ++j)
-          mbar_drain(&bars->k_full[j % C::kKStages], (j / C::kKStages) & 1);
-      }
+      // Every copy lands before the CTA can exit, whether or not the pipeline was aborted (a wait
+      // that ran out elsewhere may have ended the consumers before they saw the last tiles). In a
+      // normal run these phases have completed already.
+      for (int j = max(0, issued - C::kKStages); j < issued; ++j)
+        mbar_drain(&bars->k_full[j % C::kKStages], (j / C::kKStages) & 1, p.err);
     }
   } else if (warp == kVProducerWarp) {
     // ------------------------------ V producer --------------------------------------------
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < w.nt; ++j) {
         const int st = j % C::kVStages;
-        if (j >= C::kVStages && !mbar_wait(&bars->v_empty[st], ((j / C::kVStages) - 1) & 1, abort, p.err)) break;
+        if (j >= C::kVStages && !mbar_wait(&bars->v_empty[st], ((j / C::kVStages) - 1) & 1, abort, p.err, wl)) break;
         Tile t[C::kCPT];
         int n_present = 0;
 #pragma unroll
@@ -430,17 +431,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = j + 1;
       }
-      if (*abort) {
-        for (int j = max(0, issued - C::kVStages); j < issued; ++j)
-          mbar_drain(&bars->v_full[j % C::kVStages], (j / C::kVStages) & 1);
-      }
+      for (int j = max(0, issued - C::kVStages); j < issued; ++j)
+        mbar_drain(&bars->v_full[j % C::kVStages], (j / C::kVStages) & 1, p.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer (one lane) ---------------------------------
     // tcgen05.mma issue blocks while the tensor pipe is busy, so the tensor core idles whenever
     // this thread does anything else: it only waits on barriers and issues.
     if (lane == 0) {
-      bool ok = mbar_wait(&bars->q_ready, 0, abort, p.err);
+      bool ok = mbar_wait(&bars->q_ready, 0, abort, p.err, wl);
       tc_fence_after();
       // Descriptors are built once: a descriptor's low 14 bits hold its address >> 4, and shared
       // addresses stay below 256 KB, so adding a byte offset >> 4 moves it without carrying out of
@@ -472,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int jp = 0; ok && jp < w.nt; ++jp) {
         while (ok && next_s <= jp) {
-          ok = mbar_wait(&bars->k_full[next_s % C::kKStages], (next_s / C::kKStages) & 1, abort, p.err);
+          ok = mbar_wait(&bars->k_full[next_s % C::kKStages], (next_s / C::kKStages) & 1, abort, p.err, wl);
           if (ok) issue_s(next_s++);
         }
         while (ok && next_s < w.nt && next_s <= jp + C::kSBufs - 1 &&
@@ -482,12 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O_h += P_h V_h for tile jp over the keys [h kKH, (h + 1) kKH) of warpgroup h, which has
         // zeroed the V rows of its keys that lie outside every query's range before arriving.
         const int st = jp % C::kVStages;
-        ok = mbar_wait(&bars->v_full[st], (jp / C::kVStages) & 1, abort, p.err);
+        ok = mbar_wait(&bars->v_full[st], (jp / C::kVStages) & 1, abort, p.err, wl);
         if (!ok) break;
         const uint64_t vd = vdesc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
         const int sb = jp % C::kSBufs;
         for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait(&bars->p_full[sb][h], (jp / C::kSBufs) & 1, abort, p.err);
+          ok = mbar_wait(&bars->p_full[sb][h], (jp / C::kSBufs) & 1, abort, p.err, wl);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -504,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every MMA issued above completes before TMEM is freed.
       mma_commit(&bars->drain);
-      mbar_drain(&bars->drain, 0);
+      mbar_drain(&bars->drain, 0, p.err);
     }
     __syncwarp();
   } else {
@@ -549,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < w.nt; ++j) {
       const int sb = j % C::kSBufs;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err, wl));
       if (!ok) break;
       tc_fence_after();
       // The tile's geometry comes from the K producer through its ring. The entry is rewritten
@@ -558,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warpgroup's P of that tile. So the entry is still this tile's, and its barrier is not a
       // phase ahead.
       const int gs = j % kGeo;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[gs], (j / kGeo) & 1, abort, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[gs], (j / kGeo) & 1, abort, p.err, wl));
       if (!ok) break;
       Tile t;
       t.base = bars->tile_base[gs][cw];
@@ -607,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // even tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after, so the parity
           // wait for phase (j-1)/2 is exact.
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err));
+                          mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err, wl));
           if (!ok) break;
           tc_fence_after();
           const float a = need_o ? alpha : 1.f;
@@ -648,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tensor core, so the V rows of this half's such keys are zeroed (whole 128-byte rows:
         // the swizzle permutes 16-byte chunks within a row) before P.V reads them.
         const int sv_st = j % C::kVStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[sv_st], (j / C::kVStages) & 1, abort, p.err));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[sv_st], (j / C::kVStages) & 1, abort, p.err, wl));
         if (!ok) break;
         constexpr int kTPR = 128 / KH;                 // threads per key row
         constexpr int kPerT = C::kBoxes * 8 / kTPR;    // 16-byte chunks each of them zeroes
@@ -673,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bars->xm[wg][mrow] = l_half > 0.f ? m_ref : -INFINITY;
       bars->xl[wg][mrow] = l_half;
       mbar_arrive(&bars->xchg_l[quarter]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg_l[quarter], 0, abort, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg_l[quarter], 0, abort, p.err, wl));
       if (ok) {
         m_w[0] = bars->xm[0][mrow];
         m_w[1] = bars->xm[1][mrow];
@@ -688,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A parity wait on o_full cannot tell phase nt-1 from nt-3 when P.V_{nt-2} is still running,
     // so the last P.V has a barrier of its own.
     if (ok && w.nt > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort, p.err, wl));
       tc_fence_after();
     }
     if constexpr (MERGE) {

@@ -43,6 +43,7 @@ struct AttnParams {
   uint16_t* out;              // [T][Hq][d]
   float* lse;                 // [T][Hq] or null
   int token_cap;              // host bound on cu_q[B]
+  unsigned long long wait_limit_ns;  // pipeline waits give up after this long (0 = the default)
   int* err;
 };
 

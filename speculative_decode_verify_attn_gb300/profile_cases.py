@@ -9,7 +9,8 @@ CASE:
   accept     argmax + acceptance over 17 x 131072 fp32 logits
   select     residency top-128 of 4096 chunks
 Each repetition writes a 256 MiB buffer first, so the kernel reads HBM, not L2. The device
-holds well under 1 GiB in every case.
+holds under 1 GiB in every case; the largest is full256k, with 512 MiB of K/V beside the
+256 MiB flush buffer.
 """
 from __future__ import annotations
 

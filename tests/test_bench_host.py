@@ -74,19 +74,23 @@ def test_reference_arm_prints_its_line():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
     # at least 3 untimed warm-up steps, whatever was asked; the timed steps asked for, within the budget
     assert line["warmup"] >= 3 and line["steps"] == 1
+    # each step is a whole 40-layer pass, timed: the line's time per step and per layer agree
+    assert abs(line["ms_per_step"] * 1000 / 40 - line["value"]) <= 1e-3 * line["value"] + 1e-3
+    assert line["ms_per_step"] / 1000 <= line["config"]["timed_s"] + 0.01   # timed_s is rounded
 
 
 def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
-    """roofline.traffic comes from the committed ncu summary only while the kernel source is the
-    one the counters were taken on."""
+    """A kernel's traffic comes from its committed ncu summary only while the kernel source is
+    the one the counters were taken on."""
     src = tmp_path / "attend.cu"
     src.write_bytes(b"kernel v1")
     import hashlib
     h = hashlib.sha256(b"kernel v1").hexdigest()[:16]
     prof = tmp_path / "p.md"
     prof.write_text(f"# x\n\ntraffic_bytes: 123\nsource_sha256_16: {h}\n")
-    monkeypatch.setattr(bench, "ATTEND_SRC", str(src))
-    monkeypatch.setattr(bench, "PROFILE_8K", str(prof))
-    assert bench.profiled_traffic() == 123
+    monkeypatch.setattr(bench, "CSRC", str(tmp_path))
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    assert bench.profiled_traffic("p.md", "attend.cu") == 123
     src.write_bytes(b"kernel v2")
-    assert bench.profiled_traffic() is None
+    assert bench.profiled_traffic("p.md", "attend.cu") is None
+    assert bench.profiled_traffic("missing.md", "attend.cu") is None
