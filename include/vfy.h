@@ -109,14 +109,28 @@ VFY_API unsigned long long vfy_launch_count(const vfy_ctx* ctx);
  * through the combine kernel. */
 VFY_API vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits);
 
-/* Set the time limit of the attention kernels' pipeline waits (each wait for a copy, an MMA or
- * another warp's step), in nanoseconds; 0 restores the default of 2 s. Diagnostic and test knob:
- * a wait that runs out sets VFY_EDEVICE_TIMEOUT in the device error word, the kernel lets the
- * copies and MMAs it issued land (with the default limit), frees its tensor memory and returns;
- * that call's outputs are then undefined. The context stays usable: vfy_get_status reports and
- * clears the error, and later calls produce correct results. A limit of a few nanoseconds makes
- * the first wait that is not already complete run out. Applies to calls enqueued afterwards. */
-VFY_API vfy_status vfy_set_wait_limit(vfy_ctx* ctx, uint64_t limit_ns);
+/* Test of the timeout path (0, the default, turns it off). With limit_ns != 0, every CTA of
+ * the attention kernels enqueued afterwards first waits on a barrier that nothing completes, for
+ * limit_ns nanoseconds. That wait runs out exactly as a pipeline wait that ran out would: it sets
+ * VFY_EDEVICE_TIMEOUT in the device error word and the abort flag, the CTA's other waits give up,
+ * the copies and MMAs it issued land (under the default limit), it frees its tensor memory and
+ * returns; the call's outputs are undefined. The context stays usable: vfy_get_status reports and
+ * clears the error, and calls enqueued after the test is turned off produce correct results. No
+ * GPU fault, trap or hang is involved. */
+VFY_API vfy_status vfy_test_wait_timeout(vfy_ctx* ctx, uint64_t limit_ns);
+
+/* Declare (1) or withdraw (0, the default) that the per-step metadata the attention calls of
+ * this context read -- cu_q, seq_len, ring_offset, resident_ids, resident_slots, cu_resident --
+ * is written only by work that has completed before those calls' kernels start: host copies made
+ * before the calls are enqueued, or kernels joined to the stream through an event wait or a
+ * synchronisation. Not by a kernel earlier on the same stream: under programmatic dependent
+ * launch a kernel starts while the kernels before it still run. The attention kernels then read
+ * that metadata before they wait for the previous kernel, which takes one memory round trip per
+ * layer off the critical path. Q, the K/V data and the resident lists' entries beyond the
+ * per-sequence offsets are read after that wait. The 40-layer
+ * pass meets the condition (its residency lists come from a side stream that the layer chain
+ * joins by events). Applies to calls enqueued afterwards. */
+VFY_API vfy_status vfy_set_stable_metadata(vfy_ctx* ctx, int stable);
 
 /*
  * vfy_select_resident -- chunk-residency top-k and slot reconciliation.

@@ -27,7 +27,8 @@ struct vfy_ctx {
   int swa_splits;
   unsigned long long launches;   // kernels enqueued through this context
   int row_tiles;                 // ceil(max_queries_per_seq * G / 128)
-  unsigned long long wait_limit_ns;   // attention pipeline waits (0 = the default)
+  unsigned long long timeout_test_ns;   // see vfy_test_wait_timeout
+  int stable_metadata;                // see vfy_set_stable_metadata
 };
 
 namespace {
@@ -220,9 +221,15 @@ vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits) {
   return VFY_OK;
 }
 
-vfy_status vfy_set_wait_limit(vfy_ctx* ctx, uint64_t limit_ns) {
+vfy_status vfy_test_wait_timeout(vfy_ctx* ctx, uint64_t limit_ns) {
   VFY_REQUIRE(ctx != nullptr);
-  ctx->wait_limit_ns = limit_ns;
+  ctx->timeout_test_ns = limit_ns;
+  return VFY_OK;
+}
+
+vfy_status vfy_set_stable_metadata(vfy_ctx* ctx, int stable) {
+  VFY_REQUIRE(ctx != nullptr && (stable == 0 || stable == 1));
+  ctx->stable_metadata = stable;
   return VFY_OK;
 }
 
@@ -437,7 +444,8 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   p.scale_log2 = ctx->scale * 1.4426950408889634f;
   p.part_o = ctx->part_o;
   p.part_ml = ctx->part_ml;
-  p.wait_limit_ns = ctx->wait_limit_ns;
+  p.timeout_test_ns = ctx->timeout_test_ns;
+  p.stable_metadata = ctx->stable_metadata;
   p.err = ctx->err;
   // Full-layer splits over many resident chunks take wide tiles (their combine is a small part
   // of a long split). Otherwise up to kMaxClusterSplits splits (and no more than one GPC holds)

@@ -53,6 +53,7 @@ constexpr int kPrefetch = 6;      // tiles prefetched into L2 beyond the shared-
 // A row keeps a stale reference maximum until a tile's maximum exceeds it by this much (log2
 // units); then O and l are rescaled. The result is exact either way: O and l share the reference.
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kBarsBytes = 4096;  // shared memory reserved for the barrier block (Bars)
 
 // MERGE: the splits of one (b, h) form a cluster and merge in the kernel. Every CTA then keeps a
 // receive area where the other splits store their partial rows: for the block rows it owns (rows
@@ -83,7 +84,7 @@ struct Cfg {
   static constexpr int kRecvOffset = kQBytes + (kKStages + kVStages) * kTileBytes;
   static constexpr int kRecvMlOffset = kRecvOffset + (MERGE ? kRecvEntries * HD * 4 : 0);
   static constexpr int kBarOffset = kRecvMlOffset + (MERGE ? kRecvEntries * 8 : 0);
-  static constexpr int kSmemBytes = kBarOffset + 4096 + 1024;
+  static constexpr int kSmemBytes = kBarOffset + kBarsBytes + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -100,6 +101,7 @@ struct Bars {
   uint64_t o_done;     // one phase, after the last P.V MMA (the epilogue waits on it)
   uint64_t q_ready;
   uint64_t drain;
+  uint64_t never;       // no thread ever arrives: the timeout test's wait
   uint64_t xchg_l[4];   // per lane quarter: the two halves' (m, l) at the end
   uint32_t tmem_base;
   int abort;
@@ -110,7 +112,7 @@ struct Bars {
   float xl[2][128];
   float2 sml[128];        // cluster merge: this split's (m, l) per block row
 };
-static_assert(sizeof(Bars) <= 4096, "barrier block overflows its reservation");
+static_assert(sizeof(Bars) <= kBarsBytes, "barrier block overflows its reservation");
 
 // The per-CTA work item.
 struct Work {
@@ -313,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_ready, kSoftmaxThreads);
     for (int i = 0; i < 4; ++i) mbar_init(&bars->xchg_l[i], 64);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->never, 1);
     bars->abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
@@ -327,13 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort = &bars->abort;
-  const WaitLimit wl = make_wait_limit(p.wait_limit_ns);
 
   // Let the next kernel in the stream launch now: its prologue overlaps this kernel, and its
   // griddepcontrol.wait still waits for this grid to complete.
   pdl_launch_dependents();
-  pdl_wait();
+  // The work item comes from per-step metadata. When the caller has declared that metadata
+  // stable (written only by work that completed before this kernel started), it is read before
+  // waiting for the previous kernel, off the critical path.
+  if (!p.stable_metadata) pdl_wait();
   const Work w = make_work<RING, C::kCPT>(p);
+  if (p.stable_metadata) pdl_wait();
   if (w.bad && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, kErrDeviceInput);
 
   const uint32_t idesc_s = idesc_bf16_f32(128, C::kKT, 0, 0);
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool reported = false;
       for (int j = 0; j < w.nt; ++j) {
         const int st = j % C::kKStages;
-        if (j >= C::kKStages && !mbar_wait(&bars->k_empty[st], ((j / C::kKStages) - 1) & 1, abort, p.err, wl)) break;
+        if (j >= C::kKStages && !mbar_wait(&bars->k_empty[st], ((j / C::kKStages) - 1) & 1, abort, p.err)) break;
         Tile t[C::kCPT];
         int n_present = 0;
         bool zero = false;
@@ -412,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < w.nt; ++j) {
         const int st = j % C::kVStages;
-        if (j >= C::kVStages && !mbar_wait(&bars->v_empty[st], ((j / C::kVStages) - 1) & 1, abort, p.err, wl)) break;
+        if (j >= C::kVStages && !mbar_wait(&bars->v_empty[st], ((j / C::kVStages) - 1) & 1, abort, p.err)) break;
         Tile t[C::kCPT];
         int n_present = 0;
 #pragma unroll
@@ -439,7 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tcgen05.mma issue blocks while the tensor pipe is busy, so the tensor core idles whenever
     // this thread does anything else: it only waits on barriers and issues.
     if (lane == 0) {
-      bool ok = mbar_wait(&bars->q_ready, 0, abort, p.err, wl);
+      // Test of the timeout path (off unless asked for): one bounded wait on a barrier that
+      // nothing completes runs out, and the CTA takes the path of any wait that ran out.
+      if (p.timeout_test_ns != 0) mbar_wait_limit(&bars->never, 0, p.timeout_test_ns, abort, p.err);
+      bool ok = !*abort && mbar_wait(&bars->q_ready, 0, abort, p.err);
       tc_fence_after();
       // Descriptors are built once: a descriptor's low 14 bits hold its address >> 4, and shared
       // addresses stay below 256 KB, so adding a byte offset >> 4 moves it without carrying out of
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int jp = 0; ok && jp < w.nt; ++jp) {
         while (ok && next_s <= jp) {
-          ok = mbar_wait(&bars->k_full[next_s % C::kKStages], (next_s / C::kKStages) & 1, abort, p.err, wl);
+          ok = mbar_wait(&bars->k_full[next_s % C::kKStages], (next_s / C::kKStages) & 1, abort, p.err);
           if (ok) issue_s(next_s++);
         }
         while (ok && next_s < w.nt && next_s <= jp + C::kSBufs - 1 &&
@@ -481,12 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O_h += P_h V_h for tile jp over the keys [h kKH, (h + 1) kKH) of warpgroup h, which has
         // zeroed the V rows of its keys that lie outside every query's range before arriving.
         const int st = jp % C::kVStages;
-        ok = mbar_wait(&bars->v_full[st], (jp / C::kVStages) & 1, abort, p.err, wl);
+        ok = mbar_wait(&bars->v_full[st], (jp / C::kVStages) & 1, abort, p.err);
         if (!ok) break;
         const uint64_t vd = vdesc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
         const int sb = jp % C::kSBufs;
         for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait(&bars->p_full[sb][h], (jp / C::kSBufs) & 1, abort, p.err, wl);
+          ok = mbar_wait(&bars->p_full[sb][h], (jp / C::kSBufs) & 1, abort, p.err);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -548,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < w.nt; ++j) {
       const int sb = j % C::kSBufs;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err, wl));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
       // The tile's geometry comes from the K producer through its ring. The entry is rewritten
@@ -557,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warpgroup's P of that tile. So the entry is still this tile's, and its barrier is not a
       // phase ahead.
       const int gs = j % kGeo;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[gs], (j / kGeo) & 1, abort, p.err, wl));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[gs], (j / kGeo) & 1, abort, p.err));
       if (!ok) break;
       Tile t;
       t.base = bars->tile_base[gs][cw];
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // even tiles o_full[h][(j-1) & 1] is in phase (j-1)/2 or the one after, so the parity
           // wait for phase (j-1)/2 is exact.
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err, wl));
+                          mbar_wait(&bars->o_full[wg][(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.err));
           if (!ok) break;
           tc_fence_after();
           const float a = need_o ? alpha : 1.f;
@@ -647,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tensor core, so the V rows of this half's such keys are zeroed (whole 128-byte rows:
         // the swizzle permutes 16-byte chunks within a row) before P.V reads them.
         const int sv_st = j % C::kVStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[sv_st], (j / C::kVStages) & 1, abort, p.err, wl));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[sv_st], (j / C::kVStages) & 1, abort, p.err));
         if (!ok) break;
         constexpr int kTPR = 128 / KH;                 // threads per key row
         constexpr int kPerT = C::kBoxes * 8 / kTPR;    // 16-byte chunks each of them zeroes
@@ -672,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bars->xm[wg][mrow] = l_half > 0.f ? m_ref : -INFINITY;
       bars->xl[wg][mrow] = l_half;
       mbar_arrive(&bars->xchg_l[quarter]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg_l[quarter], 0, abort, p.err, wl));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->xchg_l[quarter], 0, abort, p.err));
       if (ok) {
         m_w[0] = bars->xm[0][mrow];
         m_w[1] = bars->xm[1][mrow];
@@ -687,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A parity wait on o_full cannot tell phase nt-1 from nt-3 when P.V_{nt-2} is still running,
     // so the last P.V has a barrier of its own.
     if (ok && w.nt > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort, p.err, wl));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort, p.err));
       tc_fence_after();
     }
     if constexpr (MERGE) {

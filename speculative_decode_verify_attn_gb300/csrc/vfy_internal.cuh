@@ -43,7 +43,9 @@ struct AttnParams {
   uint16_t* out;              // [T][Hq][d]
   float* lse;                 // [T][Hq] or null
   int token_cap;              // host bound on cu_q[B]
-  unsigned long long wait_limit_ns;  // pipeline waits give up after this long (0 = the default)
+  unsigned long long timeout_test_ns;  // != 0: each CTA first waits that long on a barrier
+                                       // nothing completes (the timeout path's test)
+  int stable_metadata;        // read the work item before the dependency wait
   int* err;
 };
 

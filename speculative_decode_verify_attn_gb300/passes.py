@@ -75,7 +75,7 @@ class VerifyPass:
     """Single-sequence 256K pass (one replica per GPU)."""
 
     def __init__(self, workload: synth.Workload, device: int = 0, seed: int = 0, all_resident: bool = False,
-                 match_prob: float = 0.56):
+                 match_prob: float = 0.56, stable_metadata: bool = True):
         assert workload.num_seqs == 1
         self.w = workload
         self.dev = torch.device("cuda", device)
@@ -97,6 +97,10 @@ class VerifyPass:
 
         self.ctx = vfy.vfy_create(hq, hkv, d, window=synth.WINDOW, ring_len=synth.RING, max_seqs=1,
                                   max_queries_per_seq=self.q, max_splits=64, device=device)
+        # The pass's metadata (lengths, offsets, block offsets) is set before any step, and its
+        # residency lists come from the paging stream, which the layer chain joins through events:
+        # every kernel that writes them has completed before a layer that reads them starts.
+        vfy.vfy_set_stable_metadata(self.ctx, stable_metadata)
         # --- per-step residency inputs ---
         self.rot = synth.rotating_residency(rng, self.n_chunks, self.k, workload.pagein_per_step or 16,
                                             self.L, self.q) if not all_resident else None

@@ -16,7 +16,7 @@ VFY_OK, VFY_EINVAL, VFY_ECUDA, VFY_ENOMEM, VFY_EUNSUPPORTED, VFY_EDEVICE_INPUT, 
 EXPORTS = ("vfy_create", "vfy_destroy", "vfy_get_status", "vfy_strerror", "vfy_set_splits",
            "vfy_select_resident", "vfy_page_in", "vfy_attend_full", "vfy_attend_swa", "vfy_accept",
            "vfy_accept_static", "vfy_launch_count", "vfy_append_full", "vfy_append_swa",
-           "vfy_gate_depths", "vfy_set_wait_limit")
+           "vfy_gate_depths", "vfy_test_wait_timeout", "vfy_set_stable_metadata")
 
 
 class VfyError(RuntimeError):
@@ -57,7 +57,8 @@ def lib() -> ctypes.CDLL:
         L.vfy_strerror.argtypes = [_I]
         L.vfy_strerror.restype = ctypes.c_char_p
         L.vfy_set_splits.argtypes = [_P, _I, _I]
-        L.vfy_set_wait_limit.argtypes = [_P, ctypes.c_uint64]
+        L.vfy_test_wait_timeout.argtypes = [_P, ctypes.c_uint64]
+        L.vfy_set_stable_metadata.argtypes = [_P, _I]
         L.vfy_select_resident.argtypes = [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
         L.vfy_page_in.argtypes = [_P, _P, _P, ctypes.c_int64, _P, _P, _I, _P, _P, _I, _I, _P]
         L.vfy_attend_full.argtypes = [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P]
@@ -185,9 +186,16 @@ def vfy_set_splits(ctx: Context, full_splits: int = 0, swa_splits: int = 0):
     _check(lib().vfy_set_splits(ctx.handle, full_splits, swa_splits), "vfy_set_splits")
 
 
-def vfy_set_wait_limit(ctx: Context, limit_ns: int = 0):
-    """Time limit of the attention kernels' pipeline waits in ns (0 = the default, 2 s)."""
-    _check(lib().vfy_set_wait_limit(ctx.handle, int(limit_ns)), "vfy_set_wait_limit")
+def vfy_test_wait_timeout(ctx: Context, limit_ns: int = 0):
+    """Test of the timeout path: every attention CTA enqueued afterwards first runs one wait of
+    limit_ns that cannot complete (0 turns the test off). See include/vfy.h."""
+    _check(lib().vfy_test_wait_timeout(ctx.handle, int(limit_ns)), "vfy_test_wait_timeout")
+
+
+def vfy_set_stable_metadata(ctx: Context, stable: bool = True):
+    """Declare that this context's per-step attention metadata is final before its kernels start
+    (see include/vfy.h); the kernels then read it before waiting for the previous kernel."""
+    _check(lib().vfy_set_stable_metadata(ctx.handle, 1 if stable else 0), "vfy_set_stable_metadata")
 
 
 def vfy_select_resident(ctx: Context, scores, cu_chunks, num_seqs: int, max_chunks_per_seq: int, k: int,

@@ -1,12 +1,12 @@
 """Failure detection without a GPU fault: every wait of the attention pipeline is bounded, and a
 wait that runs out is reported through the context's error word while the context stays usable.
 
-The test shortens the pipeline waits' limit (vfy_set_wait_limit) to 1 ns, so that the first wait
-whose phase is not already complete runs out; copies and MMAs in flight still drain under the
-default limit. vfy_get_status must then say VFY_EDEVICE_TIMEOUT, and the next call, with the
-default limit restored, must return VFY_OK and match the oracle. Each attention variant is
-covered: a full layer through the combine kernel (narrow and wide tiles) and a window layer that
-merges its splits in a thread-block cluster."""
+The test (vfy_test_wait_timeout) has every CTA of the next attention call wait 2 us on a barrier
+that nothing completes: a flag nothing sets. That wait runs out, the CTA's other waits give up,
+copies and MMAs in flight drain under the default limit. vfy_get_status must then say
+VFY_EDEVICE_TIMEOUT, and the next call, with the test off, must return VFY_OK and match the
+oracle. Each attention variant is covered: a full layer through the combine kernel (narrow and
+wide tiles) and a window layer that merges its splits in a thread-block cluster."""
 import numpy as np
 import pytest
 
@@ -50,11 +50,11 @@ def test_full_layer_wait_timeout_is_reported_and_recovered(env, splits):
     try:
         vfy.vfy_set_splits(ctx, splits, 0)
         assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
-        vfy.vfy_set_wait_limit(ctx, 1)
+        vfy.vfy_test_wait_timeout(ctx, 2000)
         H.attend_full(ctx, qb, [0, 17], kp, vp, ids, slots, [0, k], [L])
         assert vfy.vfy_get_status(ctx) == vfy.VFY_EDEVICE_TIMEOUT
         assert vfy.vfy_get_status(ctx) == vfy.VFY_OK          # read and cleared
-        vfy.vfy_set_wait_limit(ctx, 0)
+        vfy.vfy_test_wait_timeout(ctx, 0)
         got, lse = H.attend_full(ctx, qb, [0, 17], kp, vp, ids, slots, [0, k], [L])
         assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
         ref, rlse = O.attend_full_seq(qb, kp, vp, ids, slots, L)
@@ -75,10 +75,10 @@ def test_window_layer_wait_timeout_is_reported_and_recovered(env):
     qb = synth.normal_bf16(rng, (17, s.num_q_heads, s.head_dim))
     ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, max_queries_per_seq=17, device=0)
     try:
-        vfy.vfy_set_wait_limit(ctx, 1)
+        vfy.vfy_test_wait_timeout(ctx, 2000)
         H.attend_swa(ctx, qb, [0, 17], kr, vr, [phi], [L])
         assert vfy.vfy_get_status(ctx) == vfy.VFY_EDEVICE_TIMEOUT
-        vfy.vfy_set_wait_limit(ctx, 0)
+        vfy.vfy_test_wait_timeout(ctx, 0)
         got, lse = H.attend_swa(ctx, qb, [0, 17], kr, vr, [phi], [L])
         assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
         ref, rlse = O.attend_ring_seq(qb, kr[0], vr[0], phi, L, synth.WINDOW)
