@@ -473,6 +473,7 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   cp.max_q = c.max_queries_per_seq;
   cp.row_tiles = ctx->row_tiles;
   cp.token_cap = num_seqs * c.max_queries_per_seq;
+  cp.stable_metadata = ctx->stable_metadata;
   cp.part_o = ctx->part_o;
   cp.part_ml = ctx->part_ml;
   cp.out = out;

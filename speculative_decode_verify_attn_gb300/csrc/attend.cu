@@ -863,7 +863,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   __shared__ float s_l[4];
   __shared__ float s_acc[4][HD];
   pdl_launch_dependents();
-  pdl_wait();
+  // The row's sequence comes from per-step metadata: read before the dependency wait when the
+  // caller has declared it stable, after it otherwise. The partials are read after it.
+  if (!p.stable_metadata) pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = static_cast<int>(blockIdx.x / p.hq);
   const int hq = static_cast<int>(blockIdx.x % p.hq);
@@ -872,13 +874,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int total = p.cu_q[p.num_seqs];
   int b = 0;
   int c0 = p.cu_q[0], c1 = p.cu_q[1], len = p.seq_len[0];
-  if (t >= p.token_cap || t >= total) return;
-  if (p.num_seqs > 1) {
+  if (p.num_seqs > 1 && t < p.token_cap && t < total) {
     while (b + 1 < p.num_seqs && p.cu_q[b + 1] <= t) ++b;
     c0 = p.cu_q[b];
     c1 = p.cu_q[b + 1];
     len = p.seq_len[b];
   }
+  if (p.stable_metadata) pdl_wait();
+  if (t >= p.token_cap || t >= total) return;
   const int i = t - c0;
   const int nq = c1 - c0;
   if (i < 0 || nq < 0 || nq > p.max_q || len < nq) return;   // skipped by the attention kernel too

@@ -62,6 +62,7 @@ struct CombineParams {
   int max_q;
   int row_tiles;
   int token_cap;              // host bound on cu_q[B]
+  int stable_metadata;        // read cu_q / seq_len before the dependency wait
   const float* part_o;
   const float* part_ml;
   uint16_t* out;              // [T][Hq][d]
