@@ -47,9 +47,12 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
   __shared__ unsigned long long warp_best[kThreads / 32];
   __shared__ bool is_last;
   pdl_launch_dependents();   // the next kernel may launch; it still waits for this grid
-  pdl_wait();
-  const int row = blockIdx.y;
+  // The row count is per-step metadata: read before the dependency wait when the caller has
+  // declared it stable, after it otherwise. The logits are read after it.
+  if (!p.stable_metadata) pdl_wait();
   const int total_rows = p.cu_rows[p.num_seqs];
+  if (p.stable_metadata) pdl_wait();
+  const int row = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (row < total_rows && row < p.max_rows) {
@@ -118,21 +121,24 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
       continue;
     }
     const int d0 = r0 - b;   // drafts of sequence b start after the D_b' of earlier sequences
-    int n = depth;
-    for (int j0 = 0; j0 < depth; j0 += 32) {
+    // Lane j holds the greedy token of row r0 + j and draft j, both loaded in one round trip;
+    // the bonus token comes from the lane of the first mismatch (or of row D_b).
+    int n = depth, bonus = 0;
+    for (int j0 = 0; j0 <= depth; j0 += 32) {
       const int j = j0 + lane;
-      bool mismatch = false;
-      if (j < depth) {
-        const int a = unpack_index(__ldcg(p.keys + r0 + j));
-        mismatch = a != p.drafts[d0 + j];
-      }
-      const unsigned ballot = __ballot_sync(0xffffffffu, mismatch);
+      const int a = j <= depth ? unpack_index(__ldcg(p.keys + r0 + j)) : -1;
+      const int dj = j < depth ? p.drafts[d0 + j] : -1;
+      const unsigned ballot = __ballot_sync(0xffffffffu, j < depth && a != dj);
       if (ballot != 0u) {
         n = j0 + __ffs(ballot) - 1;
+        bonus = __shfl_sync(0xffffffffu, a, n - j0);
+        break;
+      }
+      if (depth < j0 + 32) {             // every draft matched: row D_b gives the bonus
+        bonus = __shfl_sync(0xffffffffu, a, depth - j0);
         break;
       }
     }
-    const int bonus = unpack_index(__ldcg(p.keys + r0 + n));
     for (int j = lane; j <= depth; j += 32) {
       int tok = -1;
       if (j < n) tok = p.drafts[d0 + j];

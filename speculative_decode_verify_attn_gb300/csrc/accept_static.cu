@@ -121,6 +121,7 @@ extern "C" vfy_status vfy_accept_static(const float* logits, int vocab, const in
   p.committed = committed;
   p.keys = st.scratch;
   p.counter = reinterpret_cast<unsigned int*>(st.scratch + kStaticMaxRows);
+  p.stable_metadata = 0;
   p.err = device_error != nullptr ? device_error : reinterpret_cast<int*>(st.scratch + kStaticMaxRows + 1);
   const bool vec4 = (vocab % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
   if (launch_accept(p, vec4, s) != cudaSuccess) {

@@ -545,6 +545,7 @@ vfy_status vfy_accept(vfy_ctx* ctx, const float* logits, int vocab, const int32_
   p.committed = committed;
   p.keys = ctx->accept_keys;
   p.counter = ctx->accept_counter;
+  p.stable_metadata = ctx->stable_metadata;
   p.err = ctx->err;
   const bool vec4 = (vocab % 4 == 0) && aligned16(logits);
   VFY_CUDA(vfy::launch_accept(p, vec4, reinterpret_cast<cudaStream_t>(stream)));

@@ -102,6 +102,7 @@ struct AcceptParams {
   int32_t* committed;
   unsigned long long* keys;   // [max_rows] workspace, zero between calls
   unsigned int* counter;      // workspace, zero between calls
+  int stable_metadata;        // read cu_rows[num_seqs] before the dependency wait
   int* err;
 };
 cudaError_t launch_accept(const AcceptParams& p, bool vec4, cudaStream_t stream);
