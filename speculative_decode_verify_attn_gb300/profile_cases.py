@@ -42,6 +42,8 @@ def main(argv=None):
     s = synth.LAGUNA
     q, L = 17, 262144
     ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, max_queries_per_seq=q, device=0)
+    # as in the 40-layer pass: the per-step metadata is set before the kernels run
+    vfy.vfy_set_stable_metadata(ctx, True)
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
     cu_q = torch.tensor([0, q], dtype=torch.int32, device=dev)
     seq_len = torch.tensor([L], dtype=torch.int32, device=dev)
