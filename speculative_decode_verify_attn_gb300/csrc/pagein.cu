@@ -3,11 +3,12 @@
 // 64-token chunks page to host RAM bit-exact").
 // The device reads the host store directly (zero-copy over the host link), so the (chunk, slot)
 // list can stay in device memory and the copy can live inside a captured CUDA graph. Grid:
-// x = list entry (sequence b, entry i < k), y = part of the chunk; entries past pagein_count[b]
-// return at once. Each thread keeps 2 x 2 independent 16-byte loads in flight. The copy is bound by
-// the host link, which a quarter of a megabyte in flight already fills (16 chunks x 256 threads x 4
-// loads); more outstanding host reads only queue in the memory system and slow the attention
-// kernels running beside the page-in, and so do more CTAs.
+// x = list entry (sequence b, entry i < k), y = half of the chunk; entries past pagein_count[b]
+// return at once. Each thread keeps 2 x 2 independent 16-byte loads in flight, so 16 chunks keep
+// half a megabyte of host reads in flight. The copy is bound by the host link's latency. Measured in
+// the 40-layer pass on GB300: two CTAs per chunk page in 20 us a pass faster than one and the pass
+// gains 2-3 us; four loads in flight per thread instead of two page in faster still but slow the
+// attention kernels beside them (the pass lost 9 us).
 #include "ptx.cuh"
 #include "vfy_internal.cuh"
 
@@ -15,7 +16,7 @@ namespace vfy {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kParts = 1;
+constexpr int kParts = 2;
 constexpr int kUnroll = 2;
 
 __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p) {

@@ -16,6 +16,7 @@ namespace vfy {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kPre = 4;      // owned chunks whose slots stay in registers (n <= 4096 at 1024 threads)
 
 __device__ __forceinline__ uint32_t score_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -95,8 +96,20 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
   const int j0 = min(n, static_cast<int>(threadIdx.x) * per);
   const int j1 = min(n, j0 + per);
 
+  // The previous slots of the first kPre owned chunks are loaded with the scores, into
+  // registers (the slot reconciliation needs them after the selection): one round trip for both.
+  int prev_r[kPre];
+#pragma unroll
+  for (int t = 0; t < kPre; ++t) prev_r[t] = j0 + t < j1 ? p.slot_of_chunk[c0 + j0 + t] : -1;
   for (int j = j0; j < j1; ++j) keys[j] = score_key(p.scores[c0 + j]);
   __syncthreads();
+  // owned chunk t's previous slot (registers for t < kPre)
+  auto prev_slot = [&](int t) {
+    int v = t < kPre ? prev_r[0] : p.slot_of_chunk[c0 + j0 + t];
+#pragma unroll
+    for (int u = 1; u < kPre; ++u) v = t == u ? prev_r[u] : v;
+    return v;
+  };
 
   // ---- radix select of the kk-th largest key ----
   uint32_t thr = 0u;
@@ -113,6 +126,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
       for (int t = 0; t < per; ++t) {
         const int j = j0 + t;
         const bool valid = j < j1 && (keys[j] & mask) == prefix;
+        if (!__any_sync(0xffffffffu, valid)) continue;   // later passes: most warps hold no candidate
         const uint32_t bin = valid ? (keys[j] >> shift) & 255u : 0xffffffffu;
         const unsigned peers = __match_any_sync(0xffffffffu, bin);
         if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
@@ -194,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
   uint32_t kept = 0u;
   for (int j = j0; j < j1; ++j) {
     if (!((chosen >> (j - j0)) & 1u)) continue;
-    const int prev = p.slot_of_chunk[c0 + j];
+    const int prev = prev_slot(j - j0);
     if (prev >= slot_base && prev < slot_base + k) {
       if (atomicExch(&keys[prev - slot_base], 1u) != 0u) s_flag = 1;   // two chunks, one slot
       kept |= 1u << (j - j0);
@@ -223,12 +237,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
   // ---- outputs ----
   int pos = pos0;
   int32_t* list = p.pagein_list + static_cast<size_t>(b) * k * 2;
+  int slot_r[kPre];                 // the new slots of the first kPre owned chunks (-1: not chosen)
+#pragma unroll
+  for (int t = 0; t < kPre; ++t) slot_r[t] = -1;
   for (int j = j0; j < j1; ++j) {
     const uint32_t bit = 1u << (j - j0);
     if (!(chosen & bit)) continue;
     int slot;
     if (kept & bit) {
-      slot = p.slot_of_chunk[c0 + j];
+      slot = prev_slot(j - j0);
     } else {
       slot = slot_base + static_cast<int>(keys[k + new_rank]);
       list[2 * new_rank] = c0 + j;
@@ -237,14 +254,26 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
     }
     p.res_ids[out0 + pos] = j;
     p.res_slots[out0 + pos] = slot;
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) slot_r[u] = j - j0 == u ? slot : slot_r[u];
     ++pos;
   }
   __syncthreads();   // every read of slot_of_chunk is done before it is rewritten
   {
     int opos = pos0;
     for (int j = j0; j < j1; ++j) {
+      const int t = j - j0;
       int v = -1;
-      if ((chosen >> (j - j0)) & 1u) v = p.res_slots[out0 + opos++];
+      if ((chosen >> t) & 1u) {
+        if (t < kPre) {
+          v = slot_r[0];
+#pragma unroll
+          for (int u = 1; u < kPre; ++u) v = t == u ? slot_r[u] : v;
+        } else {
+          v = p.res_slots[out0 + opos];
+        }
+        ++opos;
+      }
       p.slot_of_chunk[c0 + j] = v;
     }
   }
