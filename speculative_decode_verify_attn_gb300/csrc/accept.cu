@@ -54,6 +54,18 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
   if (p.stable_metadata) pdl_wait();
   const int row = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rows_done = min(total_rows, p.max_rows);
+
+  // Warp w loads sequence w's row range and its first 32 drafts now, with the logits: only the
+  // finishing CTA uses them, but which CTA finishes is known only at the end, and loading them
+  // then would add a dependent round trip to the tail of the step.
+  int f_r0 = -1, f_r1 = -1, f_draft = -1;
+  if (warp < p.num_seqs) {
+    f_r0 = p.cu_rows[warp];
+    f_r1 = p.cu_rows[warp + 1];
+    const int depth = f_r1 - f_r0 - 1;
+    if (f_r0 >= 0 && depth >= 0 && f_r1 <= rows_done && lane < depth) f_draft = p.drafts[f_r0 - warp + lane];
+  }
 
   if (row < total_rows && row < p.max_rows) {
     const int v0 = blockIdx.x * p.seg;
@@ -98,23 +110,24 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
     atomicOr(p.err, kErrDeviceInput);
   }
 
-  // Ticket: the last CTA of the grid does the acceptance.
+  // Ticket: the last CTA of the grid does the acceptance. The add has release semantics (this
+  // CTA's key is visible before its ticket); the finishing CTA acquires.
   if (threadIdx.x == 0) {
-    __threadfence();
     const unsigned int total = gridDim.x * gridDim.y;
-    const unsigned int ticket = atomicAdd(p.counter, 1u);
+    unsigned int ticket;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(p.counter) : "memory");
     is_last = (ticket == total - 1);
   }
   __syncthreads();
   if (!is_last) {
     return;
   }
-  __threadfence();
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 
-  const int rows_done = min(total_rows, p.max_rows);
   for (int b = warp; b < p.num_seqs; b += kThreads / 32) {
-    const int r0 = p.cu_rows[b];
-    const int r1 = p.cu_rows[b + 1];
+    const bool pre = b == warp;                      // this warp's preloaded sequence
+    const int r0 = pre ? f_r0 : p.cu_rows[b];
+    const int r1 = pre ? f_r1 : p.cu_rows[b + 1];
     const int depth = r1 - r0 - 1;
     if (r0 < 0 || depth < 0 || r1 > rows_done) {
       if (lane == 0) atomicOr(p.err, kErrDeviceInput);
@@ -127,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
     for (int j0 = 0; j0 <= depth; j0 += 32) {
       const int j = j0 + lane;
       const int a = j <= depth ? unpack_index(__ldcg(p.keys + r0 + j)) : -1;
-      const int dj = j < depth ? p.drafts[d0 + j] : -1;
+      const int dj = j < depth ? (pre && j0 == 0 ? f_draft : p.drafts[d0 + j]) : -1;
       const unsigned ballot = __ballot_sync(0xffffffffu, j < depth && a != dj);
       if (ballot != 0u) {
         n = j0 + __ffs(ballot) - 1;
@@ -141,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
     }
     for (int j = lane; j <= depth; j += 32) {
       int tok = -1;
-      if (j < n) tok = p.drafts[d0 + j];
+      if (j < n) tok = pre && j < 32 ? f_draft : p.drafts[d0 + j];   // lane j holds draft j
       else if (j == n) tok = bonus;
       p.committed[r0 + j] = tok;
     }
@@ -152,9 +165,9 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
   }
   __syncthreads();
   // Leave the workspace as this call found it: all keys zero, ticket zero.
+  // (The kernel's completion makes these writes visible to the next call.)
   for (int r = threadIdx.x; r < p.max_rows; r += kThreads) p.keys[r] = 0ull;
   if (threadIdx.x == 0) *p.counter = 0u;
-  __threadfence();
 }
 
 }  // namespace
