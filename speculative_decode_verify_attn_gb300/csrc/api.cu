@@ -401,10 +401,18 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   if (!ring) {
     splits = ctx->full_splits;
     if (splits == 0) {
-      // One wave of CTAs for one sequence; several waves for a batch, so that the hardware
-      // scheduler can balance sequences of different lengths.
-      const int target = ctx->num_sms * (num_seqs > 1 || ctx->row_tiles > 1 ? 4 : 1);
-      splits = ceil_div(target, static_cast<long long>(hkv) * num_seqs * ctx->row_tiles);
+      if (ctx->row_tiles > 1) {
+        // Blocks of several row tiles (prefill-shaped) have (KV head, row tile) items enough to
+        // fill the SMs with few splits, and a long split keeps the tensor pipe busier: at most one
+        // wave. Measured with 1024 queries over 128 chunks (128 items): 1 split 121 us, 2 splits
+        // 130, 3 138, 4 146, 5 (four waves) 155.
+        splits = ctx->num_sms / (hkv * num_seqs * ctx->row_tiles);
+      } else {
+        // One wave of CTAs for one sequence; several waves for a batch, so that the hardware
+        // scheduler can balance sequences of different lengths.
+        const int target = ctx->num_sms * (num_seqs > 1 ? 4 : 1);
+        splits = ceil_div(target, static_cast<long long>(hkv) * num_seqs);
+      }
       splits = clampi(splits, 1, max_res > 0 ? max_res : 1);
     }
   } else {
@@ -452,15 +460,21 @@ static vfy_status attend_common(vfy_ctx* ctx, bool ring, const uint16_t* q, cons
   // merge inside the attention kernel, as one thread-block cluster per (sequence, KV head, row
   // tile); more go through the combine.
   const bool wide = !ring && ceil_div(max_res > 0 ? max_res : 1, splits) >= vfy::kWideMinChunks;
-  const bool merge = !wide && splits <= vfy::kMaxClusterSplits && splits <= vfy::attend_merge_limit(ring, c.head_dim);
-  const vfy::AttnTiles tiles = merge ? vfy::AttnTiles::kMerge : (wide ? vfy::AttnTiles::kWide : vfy::AttnTiles::kNarrow);
-  p.out = merge ? out : nullptr;
-  p.lse = merge ? lse : nullptr;
+  // A single split of a long block writes O itself (no combine launch).
+  const bool direct = wide && splits == 1;
+  const bool merge = !direct && !wide && splits <= vfy::kMaxClusterSplits &&
+                     splits <= vfy::attend_merge_limit(ring, c.head_dim);
+  const vfy::AttnTiles tiles = merge    ? vfy::AttnTiles::kMerge
+                              : direct ? vfy::AttnTiles::kWideDirect
+                              : wide   ? vfy::AttnTiles::kWide
+                                       : vfy::AttnTiles::kNarrow;
+  p.out = merge || direct ? out : nullptr;
+  p.lse = merge || direct ? lse : nullptr;
   p.token_cap = num_seqs * c.max_queries_per_seq;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   VFY_CUDA(vfy::launch_attend(ring, c.head_dim, tiles, p, tk, tv, num_seqs, s));
   ++ctx->launches;
-  if (merge) return VFY_OK;
+  if (merge || direct) return VFY_OK;
 
   vfy::CombineParams cp;
   cp.cu_q = cu_q;

@@ -279,10 +279,11 @@ __device__ __forceinline__ uint32_t staged_offset(int r, int col) {
   return static_cast<uint32_t>((r * HD + ((c ^ ((r >> 2) & 7)) << 2) + (col & 3)) * 4);
 }
 
-template <int HD, bool RING, bool MERGE, bool WIDE>
+template <int HD, bool RING, bool MERGE, bool WIDE, bool DIRECT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
+  static_assert(!DIRECT || !MERGE, "a single split writes its output without a merge");
   using C = Cfg<HD, RING, MERGE, WIDE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -742,6 +743,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_dsmem_f2(dst, *reinterpret_cast<const float2*>(so + staged_offset<HD>(rr, lane * 2)));
         }
       }
+    } else if constexpr (DIRECT) {
+      // A single split: this CTA holds every key of its rows, so it normalises O and writes it,
+      // bf16, with the LSE; no combine follows. (A variant of its own: the same branch, untaken,
+      // in the kernel the 40-layer pass runs made its full layers 2.7 us slower.) Warpgroup h writes
+      // columns [h d/2, (h + 1) d/2). A row without an attended key gets O = 0, LSE = -inf.
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      const unsigned br = static_cast<unsigned>(r);
+      const unsigned bq = br / static_cast<unsigned>(p.group);
+      const int t = w.q0 + static_cast<int>(bq);
+      const int hq = w.h * p.group + static_cast<int>(br - bq * static_cast<unsigned>(p.group));
+      const bool wr = ok && rv && t < p.token_cap;
+      uint16_t* dst = p.out + (static_cast<size_t>(wr ? t : 0) * p.hq + hq) * HD + wg * (HD / 2);
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t o0[32], o1[32];
+        if (ok && w.nt > 0) {
+          tmem_ld32(lane_base + kColO + wg * (HD / 2) + c * 32, o0);
+          tmem_ld32(lane_base + kColO + 128 + wg * (HD / 2) + c * 32, o1);
+        }
+        if (wr) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a = 0.f, b = 0.f;
+            if (w.nt > 0 && l_sum > 0.f) {
+              a = (w0 * __uint_as_float(o0[2 * e]) + w1 * __uint_as_float(o1[2 * e])) * inv;
+              b = (w0 * __uint_as_float(o0[2 * e + 1]) + w1 * __uint_as_float(o1[2 * e + 1])) * inv;
+            }
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<uint4*>(dst + c * 32 + 2 * e) = make_uint4(pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
+        }
+      }
+      if (wr && wg == 0 && p.lse != nullptr)
+        p.lse[static_cast<size_t>(t) * p.hq + hq] =
+            l_sum > 0.f ? (m_row + __log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
     } else if (ok) {
       // warpgroup h writes columns [h d/2, (h + 1) d/2) of the merged O
       float* dst = p.part_o + (pidx * kMaxRows + lr) * HD + wg * (HD / 2);
@@ -1003,11 +1043,11 @@ static int merge_cluster_limit() {
   return limit[dev];
 }
 
-template <int HD, bool RING, bool MERGE, bool WIDE>
+template <int HD, bool RING, bool MERGE, bool WIDE, bool DIRECT = false>
 static cudaError_t launch_attend_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                    int num_seqs, cudaStream_t stream) {
   static size_t done[64] = {};
-  auto kern = attend_kernel<HD, RING, MERGE, WIDE>;
+  auto kern = attend_kernel<HD, RING, MERGE, WIDE, DIRECT>;
   constexpr int kSmem = Cfg<HD, RING, MERGE, WIDE>::kSmemBytes;
   cudaError_t e = ensure_smem_limit(kern, kSmem, done);
   if (e != cudaSuccess) return e;
@@ -1034,13 +1074,14 @@ static cudaError_t launch_attend_hd(bool ring, AttnTiles tiles, const AttnParams
   switch (tiles) {
     case AttnTiles::kMerge: return launch_attend_t<HD, false, true, false>(p, tk, tv, num_seqs, stream);
     case AttnTiles::kWide: return launch_attend_t<HD, false, false, true>(p, tk, tv, num_seqs, stream);
+    case AttnTiles::kWideDirect: return launch_attend_t<HD, false, false, true, true>(p, tk, tv, num_seqs, stream);
     default: return launch_attend_t<HD, false, false, false>(p, tk, tv, num_seqs, stream);
   }
 }
 
 cudaError_t launch_attend(bool ring, int head_dim, AttnTiles tiles, const AttnParams& p, const CUtensorMap& tk,
                           const CUtensorMap& tv, int num_seqs, cudaStream_t stream) {
-  if (ring && tiles == AttnTiles::kWide) return cudaErrorInvalidValue;
+  if (ring && (tiles == AttnTiles::kWide || tiles == AttnTiles::kWideDirect)) return cudaErrorInvalidValue;
   if (head_dim == 128) return launch_attend_hd<128>(ring, tiles, p, tk, tv, num_seqs, stream);
   return launch_attend_hd<64>(ring, tiles, p, tk, tv, num_seqs, stream);
 }

@@ -78,7 +78,9 @@ struct CombineParams {
 //           the splits and writes p.out / p.lse itself (no combine launch follows). Returns
 //           cudaErrorNotSupported, before launching anything, when such a cluster cannot be
 //           resident on this device.
-enum class AttnTiles { kNarrow, kWide, kMerge };
+//  kWideDirect  kWide with a single split: the kernel normalises O and writes p.out / p.lse
+//           itself (no combine launch)
+enum class AttnTiles { kNarrow, kWide, kMerge, kWideDirect };
 // A split of a full layer takes wide tiles from this many resident chunks on.
 constexpr int kWideMinChunks = 8;
 cudaError_t launch_attend(bool ring, int head_dim, AttnTiles tiles, const AttnParams& p, const CUtensorMap& tk,
