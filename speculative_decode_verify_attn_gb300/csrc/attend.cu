@@ -57,9 +57,12 @@ constexpr int kBarsBytes = 4096;  // shared memory reserved for the barrier bloc
 
 // MERGE: the splits of one (b, h) form a cluster and merge in the kernel. Every CTA then keeps a
 // receive area where the other splits store their partial rows: for the block rows it owns (rows
-// rank, rank + n, ...; slot k holds row rank + n k) one (m, l) pair and one fp32 O row per split,
-// at index k * n + split. k * n + split < kMaxRows + n, so kMaxRows + kMaxClusterSplits entries
-// cover every cluster size. A merging CTA processes few tiles, so it takes fewer K/V stages.
+// rank, rank + n, ...; slot k holds row rank + n k) one fp32 (m, l) pair and one bf16 O row
+// (normalised by l) per split, at index k * n + split. k * n + split < kMaxRows + n, so
+// kMaxRows + kMaxClusterSplits entries cover every cluster size. A merging CTA processes few
+// tiles, so it takes fewer K/V stages. Forwarding the rows as bf16 halved what the merge moves:
+// window layers 7.50 -> 7.30 us in their chain (the rounding, about 2^-9 of a partial, stays far
+// inside the attention tolerance).
 template <int HD, bool RING, bool MERGE, bool WIDE>
 struct Cfg {
   static_assert(!WIDE || (!RING && !MERGE), "wide tiles are for full layers without the cluster merge");
@@ -82,7 +85,7 @@ struct Cfg {
   static_assert(kColS + kSBufs * kKT <= kTmemCols, "tensor memory");
   static constexpr int kRecvEntries = kMaxRows + kMaxClusterSplits;
   static constexpr int kRecvOffset = kQBytes + (kKStages + kVStages) * kTileBytes;
-  static constexpr int kRecvMlOffset = kRecvOffset + (MERGE ? kRecvEntries * HD * 4 : 0);
+  static constexpr int kRecvMlOffset = kRecvOffset + (MERGE ? kRecvEntries * HD * 2 : 0);
   static constexpr int kBarOffset = kRecvMlOffset + (MERGE ? kRecvEntries * 8 : 0);
   static constexpr int kSmemBytes = kBarOffset + kBarsBytes + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -269,14 +272,15 @@ __device__ __forceinline__ void key_interval(const AttnParams& p, const Work& w,
   }
 }
 
-// Cluster merge: a split first stages its merged O rows in its own (then idle) K/V stages, fp32,
-// row r at r * HD floats with 16-byte chunk c at chunk c ^ ((r >> 2) & 7): the softmax lanes of a
-// warp hold rows 4 apart and write without bank conflicts, and a warp reading one row sees a
-// permutation of its chunks.
+// Cluster merge: a split first stages its merged O rows in its own (then idle) K/V stages, as bf16
+// normalised by the split's row sum: row r at r * HD * 2 bytes, 16-byte chunk ch at chunk
+// ch ^ (r mod (HD / 8)), so that the softmax lanes of a warp (consecutive rows) write one chunk
+// column without all landing in one bank group, and a warp reading one row sees a permutation of
+// its chunks.
 template <int HD>
-__device__ __forceinline__ uint32_t staged_offset(int r, int col) {
-  const int c = col >> 2;
-  return static_cast<uint32_t>((r * HD + ((c ^ ((r >> 2) & 7)) << 2) + (col & 3)) * 4);
+__device__ __forceinline__ uint32_t staged16_offset(int r, int ch) {
+  constexpr int kChunks = HD / 8;                      // 16-byte chunks (8 bf16) per row
+  return static_cast<uint32_t>(r * HD * 2 + ((ch ^ (r & (kChunks - 1))) << 4));
 }
 
 template <int HD, bool RING, bool MERGE, bool WIDE, bool DIRECT = false>
@@ -701,11 +705,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if constexpr (MERGE) {
-      // Stage the split's (m, l, unnormalised O) rows locally; a split without data for a row
-      // stages (-inf, 0) and no O. Then every softmax warp forwards whole rows, one 512-byte store
-      // per row (d = 128), into the receive area of the row's owner, split rank r % n.
+      // Stage the split's rows locally as bf16, normalised by the split's row sum l (the (m, l)
+      // pair stays fp32); a split without data for a row stages (-inf, 0) and no O. Then the
+      // softmax warps forward the rows into the receive area of each row's owner, split rank
+      // r % n: one 16-byte store per lane, 32 / (d / 8) rows per warp store.
       uint8_t* so = sK;                                // the K and V stages, idle after o_done
       if (ok && w.nt > 0) {
+        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
           uint32_t o0[32], o1[32];
@@ -713,12 +719,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(lane_base + kColO + 128 + wg * (HD / 2) + c * 32, o1);
           if (rv && l_sum > 0.f) {
 #pragma unroll
-            for (int x = 0; x < 32; x += 4)
-              *reinterpret_cast<float4*>(so + staged_offset<HD>(lr, wg * (HD / 2) + c * 32 + x)) =
-                  make_float4(w0 * __uint_as_float(o0[x]) + w1 * __uint_as_float(o1[x]),
-                              w0 * __uint_as_float(o0[x + 1]) + w1 * __uint_as_float(o1[x + 1]),
-                              w0 * __uint_as_float(o0[x + 2]) + w1 * __uint_as_float(o1[x + 2]),
-                              w0 * __uint_as_float(o0[x + 3]) + w1 * __uint_as_float(o1[x + 3]));
+            for (int x = 0; x < 32; x += 8) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float a = (w0 * __uint_as_float(o0[x + 2 * e]) + w1 * __uint_as_float(o1[x + 2 * e])) * inv;
+                const float b =
+                    (w0 * __uint_as_float(o0[x + 2 * e + 1]) + w1 * __uint_as_float(o1[x + 2 * e + 1])) * inv;
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+                pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(so + staged16_offset<HD>(lr, (wg * (HD / 2) + c * 32 + x) >> 3)) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
           }
         }
       }
@@ -726,21 +739,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kSoftmaxThreads);
       const int n = static_cast<int>(cluster_nctarank());
       const int rank = static_cast<int>(cluster_ctarank());
-      constexpr int kPer = HD / 32;
+      constexpr int kChunks = HD / 8;                  // 16-byte chunks per row
+      constexpr int kRowsPerStore = 32 / kChunks;      // rows one warp store forwards
+      const int sub = lane / kChunks, ch = lane % kChunks;
       const uint32_t recv = smem_u32(smem + C::kRecvOffset);
       const uint32_t recv_ml = smem_u32(smem + C::kRecvMlOffset);
-      for (int rr = warp; rr < w.rows; rr += kSoftmaxThreads / 32) {
-        const float2 ml = bars->sml[rr];
-        const unsigned rq = static_cast<unsigned>(rr) / static_cast<unsigned>(n);
-        const int e = static_cast<int>(rq) * n + rank;  // entry in the owner's receive area
-        const uint32_t owner = static_cast<uint32_t>(rr - static_cast<int>(rq) * n);
-        if (lane == 0) st_dsmem_f2(dsmem_addr(recv_ml + e * 8, owner), ml);
-        if (ml.y > 0.f) {
-          const uint32_t dst = dsmem_addr(recv + (e * HD + lane * kPer) * 4, owner);
-          if constexpr (kPer == 4)
-            st_dsmem_f4(dst, *reinterpret_cast<const float4*>(so + staged_offset<HD>(rr, lane * 4)));
-          else
-            st_dsmem_f2(dst, *reinterpret_cast<const float2*>(so + staged_offset<HD>(rr, lane * 2)));
+      for (int rb = warp * kRowsPerStore; rb < w.rows; rb += (kSoftmaxThreads / 32) * kRowsPerStore) {
+        const int rr = rb + sub;
+        if (rr < w.rows) {
+          const float2 ml = bars->sml[rr];
+          const unsigned rq = static_cast<unsigned>(rr) / static_cast<unsigned>(n);
+          const int e = static_cast<int>(rq) * n + rank;  // entry in the owner's receive area
+          const uint32_t owner = static_cast<uint32_t>(rr - static_cast<int>(rq) * n);
+          if (ch == 0) st_dsmem_f2(dsmem_addr(recv_ml + e * 8, owner), ml);
+          if (ml.y > 0.f)
+            st_dsmem_u4(dsmem_addr(recv + e * HD * 2 + ch * 16, owner),
+                        *reinterpret_cast<const uint4*>(so + staged16_offset<HD>(rr, ch)));
         }
       }
     } else if constexpr (DIRECT) {
@@ -819,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = static_cast<int>(cluster_nctarank());
     const int rank = static_cast<int>(cluster_ctarank());
     constexpr int kPer = HD / 32;                      // columns per lane
-    const float* recv = reinterpret_cast<const float*>(smem + C::kRecvOffset);
+    const uint16_t* recv = reinterpret_cast<const uint16_t*>(smem + C::kRecvOffset);
     const float2* recv_ml = reinterpret_cast<const float2*>(smem + C::kRecvMlOffset);
     for (int k = warp;; k += kThreads / 32) {
       const int r = rank + n * k;
@@ -828,8 +842,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mm = ml.y > 0.f ? ml.x : -INFINITY;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-      const float wgt = ml.y > 0.f ? ex2_approx(ml.x - mm) : 0.f;
-      float lsum = wgt * ml.y;
+      // the rows are normalised by their split's l: weight 2^(m - M) l
+      const float wgt = ml.y > 0.f ? ex2_approx(ml.x - mm) * ml.y : 0.f;
+      float lsum = wgt;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
       float acc[kPer];
@@ -842,17 +857,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < n; ++s) {
         const float ws = __shfl_sync(0xffffffffu, wgt, s);
         const bool use = ws != 0.f;
-        const float* src = recv + static_cast<size_t>(k * n + s) * HD + lane * kPer;
+        const uint16_t* src = recv + static_cast<size_t>(k * n + s) * HD + lane * kPer;
         if constexpr (kPer == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src);
-          acc[0] = use ? fmaf(ws, v.x, acc[0]) : acc[0];
-          acc[1] = use ? fmaf(ws, v.y, acc[1]) : acc[1];
-          acc[2] = use ? fmaf(ws, v.z, acc[2]) : acc[2];
-          acc[3] = use ? fmaf(ws, v.w, acc[3]) : acc[3];
+          const uint2 u = *reinterpret_cast<const uint2*>(src);
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+          acc[0] = use ? fmaf(ws, a.x, acc[0]) : acc[0];
+          acc[1] = use ? fmaf(ws, a.y, acc[1]) : acc[1];
+          acc[2] = use ? fmaf(ws, b.x, acc[2]) : acc[2];
+          acc[3] = use ? fmaf(ws, b.y, acc[3]) : acc[3];
         } else {
-          const float2 v = *reinterpret_cast<const float2*>(src);
-          acc[0] = use ? fmaf(ws, v.x, acc[0]) : acc[0];
-          acc[1] = use ? fmaf(ws, v.y, acc[1]) : acc[1];
+          const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+          acc[0] = use ? fmaf(ws, a.x, acc[0]) : acc[0];
+          acc[1] = use ? fmaf(ws, a.y, acc[1]) : acc[1];
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
