@@ -4,6 +4,8 @@
 
 CASE:
   full8k     one full-attention layer of the 256K workload: 128 of 4096 chunks resident (16 MiB)
+  prefill    a 1024-query block over the same 128 resident chunks (one split per row tile, which
+             writes its own output)
   full256k   one full-attention layer with all 4096 chunks resident (512 MiB of KV)
   swa        one window layer (512-token window, 2048-slot ring, wrapping)
   accept     argmax + acceptance over 17 x 131072 fp32 logits
@@ -30,7 +32,7 @@ from speculative_decode_verify_attn_gb300 import build, synth, vfy  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["full8k", "full256k", "swa", "accept", "select"])
+    ap.add_argument("case", choices=["full8k", "full256k", "swa", "accept", "select", "prefill"])
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args(argv)
     build.build()
@@ -40,7 +42,7 @@ def main(argv=None):
     g.manual_seed(0)
     rng = np.random.default_rng(0)
     s = synth.LAGUNA
-    q, L = 17, 262144
+    q, L = (1024 if a.case == "prefill" else 17), 262144
     ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, max_queries_per_seq=q, device=0)
     # as in the 40-layer pass: the per-step metadata is set before the kernels run
     vfy.vfy_set_stable_metadata(ctx, True)
@@ -51,7 +53,7 @@ def main(argv=None):
     out = torch.empty_like(qt)
     lse = torch.empty((q, s.num_q_heads), dtype=torch.float32, device=dev)
 
-    if a.case in ("full8k", "full256k"):
+    if a.case in ("full8k", "full256k", "prefill"):
         n = 4096 if a.case == "full256k" else 128
         kp = torch.randn((n, s.num_kv_heads, 64, s.head_dim), generator=g, device=dev, dtype=torch.bfloat16)
         vp = torch.randn_like(kp)
