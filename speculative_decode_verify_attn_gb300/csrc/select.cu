@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
   __shared__ int scan_buf[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
+  __shared__ int s_whole;       // the chosen digit's bin is taken whole: the threshold is found
   __shared__ int s_out0;
   __shared__ int s_flag;
 
@@ -160,12 +161,19 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams p) 
           }
           s_remaining = remaining - above;
           s_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - u) << shift);
+          s_whole = (u < 8 ? c[u] : 0) == remaining - above && remaining > above;
         }
       }
       __syncthreads();
       remaining = s_remaining;
       prefix = s_prefix;
       mask |= 255u << shift;
+      if (s_whole) {
+        // Every key of the bin is chosen: they are exactly the keys >= prefix among the
+        // candidates, so no lower digit is needed and no tie has to be broken.
+        remaining = 0x7fffffff;
+        break;
+      }
     }
     thr = prefix;
     take_eq = remaining;

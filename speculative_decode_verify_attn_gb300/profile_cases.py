@@ -6,6 +6,7 @@ CASE:
   full8k     one full-attention layer of the 256K workload: 128 of 4096 chunks resident (16 MiB)
   prefill    a 1024-query block over the same 128 resident chunks (one split per row tile, which
              writes its own output)
+  drafter    one layer of the drafter's context-KV ring (window 4096 in an 8192-slot ring)
   full256k   one full-attention layer with all 4096 chunks resident (512 MiB of KV)
   swa        one window layer (512-token window, 2048-slot ring, wrapping)
   accept     argmax + acceptance over 17 x 131072 fp32 logits
@@ -32,7 +33,7 @@ from speculative_decode_verify_attn_gb300 import build, synth, vfy  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["full8k", "full256k", "swa", "accept", "select", "prefill"])
+    ap.add_argument("case", choices=["full8k", "full256k", "swa", "accept", "select", "prefill", "drafter"])
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args(argv)
     build.build()
@@ -42,8 +43,10 @@ def main(argv=None):
     g.manual_seed(0)
     rng = np.random.default_rng(0)
     s = synth.LAGUNA
-    q, L = (1024 if a.case == "prefill" else 17), 262144
-    ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, max_queries_per_seq=q, device=0)
+    q, L = (1024 if a.case == "prefill" else 16 if a.case == "drafter" else 17), 262144
+    W, R = (synth.DRAFTER_WINDOW, synth.DRAFTER_RING) if a.case == "drafter" else (synth.WINDOW, synth.RING)
+    ctx = vfy.vfy_create(s.num_q_heads, s.num_kv_heads, s.head_dim, window=W, ring_len=R, max_queries_per_seq=q,
+                         device=0)
     # as in the 40-layer pass: the per-step metadata is set before the kernels run
     vfy.vfy_set_stable_metadata(ctx, True)
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
@@ -67,10 +70,10 @@ def main(argv=None):
 
         def run():
             vfy.vfy_attend_full(ctx, qt, cu_q, kp, vp, n, ids_t, slots_t, cu_res, n, seq_len, out, lse, 1)
-    elif a.case == "swa":
-        rk = torch.randn((1, s.num_kv_heads, synth.RING, s.head_dim), generator=g, device=dev, dtype=torch.bfloat16)
+    elif a.case in ("swa", "drafter"):
+        rk = torch.randn((1, s.num_kv_heads, R, s.head_dim), generator=g, device=dev, dtype=torch.bfloat16)
         rv = torch.randn_like(rk)
-        phi = synth.wrapping_ring_offset(rng, L, synth.WINDOW + q - 1, synth.RING)
+        phi = synth.wrapping_ring_offset(rng, L, W + q - 1, R)
         off = torch.tensor([phi], dtype=torch.int32, device=dev)
 
         def run():
