@@ -38,6 +38,13 @@ __device__ __forceinline__ int unpack_index(unsigned long long key) {
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull));
 }
 
+// max that returns NaN when either operand is NaN (fmaxf returns the other operand)
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
   return a > b ? a : b;
 }
@@ -82,16 +89,37 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptParams p) 
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
           if (i0 + u * kThreads < n4) v[u] = __ldcs(s4 + i0 + u * kThreads);
+          else v[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        // The round's best key without packing every entry: the largest value by a NaN-propagating
+        // max (NaN iff the round holds one), then the lowest index holding that value (a float
+        // compare: -0 == +0, the two keys' tie) or, with a NaN, the lowest NaN's index. Padding
+        // entries hold -inf at indices past the segment, so they never win a tie.
+        float m = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int i = i0 + u * kThreads;
-          if (i < n4) {
-            const int base = v0 + 4 * i;
-            const unsigned long long k01 = umax64(pack(v[u].x, base), pack(v[u].y, base + 1));
-            const unsigned long long k23 = umax64(pack(v[u].z, base + 2), pack(v[u].w, base + 3));
-            best = umax64(best, umax64(k01, k23));
+        for (int u = 0; u < kUnroll; ++u)
+          m = max_nan(m, max_nan(max_nan(v[u].x, v[u].y), max_nan(v[u].z, v[u].w)));
+        int at = 0x7fffffff;
+        if (m == m) {
+#pragma unroll
+          for (int u = kUnroll - 1; u >= 0; --u) {
+            const int base = v0 + 4 * (i0 + u * kThreads);
+            at = v[u].w == m ? base + 3 : at;
+            at = v[u].z == m ? base + 2 : at;
+            at = v[u].y == m ? base + 1 : at;
+            at = v[u].x == m ? base : at;
+          }
+        } else {
+          m = __uint_as_float(0x7fffffffu);
+#pragma unroll
+          for (int u = kUnroll - 1; u >= 0; --u) {
+            const int base = v0 + 4 * (i0 + u * kThreads);
+            at = v[u].w != v[u].w ? base + 3 : at;
+            at = v[u].z != v[u].z ? base + 2 : at;
+            at = v[u].y != v[u].y ? base + 1 : at;
+            at = v[u].x != v[u].x ? base : at;
           }
         }
+        if (at != 0x7fffffff) best = umax64(best, pack(m, at));
       }
       for (int i = v0 + 4 * n4 + threadIdx.x; i < v1; i += kThreads) best = umax64(best, pack(src[i], i));
     } else {

@@ -194,6 +194,33 @@ def test_accept_ties_nan_and_odd_vocab(H, vfy, ctx):
     assert [O.argmax_row(r) for r in logits] == torch_a
 
 
+def test_accept_ties_nan_vectorised_path(H, vfy, ctx):
+    """Vocabulary a multiple of 4 (16-byte loads): ties inside one 16-byte word, inside one thread's
+    round of loads and across CTAs, signed zeros, infinities, NaN and a maximum in the last entry."""
+    V = 131072
+    rows = 10
+    logits = np.full((rows, V), -1.0, np.float32)
+    logits[0, [9, 10]] = 50.0                          # one 16-byte word -> 9
+    logits[1, [1 + 4 * 256 * 3, 1, 70001]] = 50.0      # one thread's round and another CTA -> 1
+    logits[2, [40, 41]] = [-0.0, 0.0]                  # signed zeros tie -> 40
+    logits[3, [50, 51]] = [0.0, -0.0]                  # -> 50
+    logits[4, [7 + 1024, 7, 100]] = [np.nan, np.nan, np.inf]   # first NaN -> 7
+    logits[5, [3, 131000]] = [np.inf, np.inf]          # -> 3
+    logits[6] = -np.inf                                # -> 0
+    logits[7, 131071] = 2.0                            # the last entry -> 131071
+    logits[8] = -0.0                                   # all -0 -> 0
+    logits[9, [23, 24, 131068]] = [np.nan, 5.0, np.nan]   # NaN in a word's last lane -> 23
+    want = [9, 1, 40, 50, 7, 3, 0, 131071, 0, 23]
+    assert [O.argmax_row(r) for r in logits] == want
+    drafts = np.array(want[:-1], np.int32)
+    drafts[4] = 8                                      # the first mismatch is draft 4
+    n, bonus, committed = H.accept(ctx, logits, drafts, [0, rows])
+    rn, rb, rc = O.accept(logits, drafts, [0, rows])
+    assert n.tolist() == rn.tolist() == [4]
+    assert bonus.tolist() == rb.tolist() == [7]
+    assert committed.tolist() == rc.tolist()
+
+
 def test_accept_ragged_batch_and_repeat_calls(H, vfy, ctx):
     """Eight sequences, depths from {2,4,8,11,16} and one depth 0; the second call must not see the
     first call's state."""
