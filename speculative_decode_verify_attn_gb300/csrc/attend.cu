@@ -562,20 +562,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < w.nt; ++j) {
       const int sb = j % C::kSBufs;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err));
-      if (!ok) break;
-      tc_fence_after();
-      // The tile's geometry comes from the K producer through its ring. The entry is rewritten
-      // for tile j + kGeo only after S_{j + kGeo - kKStages} has read its K; that S needed its
-      // buffer back from P.V of tile j + kGeo - kKStages - kSBufs >= j, which waits for this
-      // warpgroup's P of that tile. So the entry is still this tile's, and its barrier is not a
-      // phase ahead.
+      // The tile's geometry comes from the K producer through its ring, written before the tile's
+      // copies are issued, so it is read (with this row's key interval) while S_j is computed.
+      // The entry is rewritten for tile j + kGeo only after S_{j + kGeo - kKStages} has read its
+      // K; that S needed its buffer back from P.V of tile j + kGeo - kKStages - kSBufs >= j, which
+      // waits for this warpgroup's P of that tile. So the entry is still this tile's, and its
+      // barrier is not a phase ahead.
       const int gs = j % kGeo;
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->geo_full[gs], (j / kGeo) & 1, abort, p.err));
       if (!ok) break;
       Tile t;
       t.base = bars->tile_base[gs][cw];
       t.valid = bars->tile_valid[gs][cw] != 0;
+      int klo = 0, khi = kChunk - 1;
+      if (rv) key_interval<RING>(p, w, t, p_i, &klo, &khi);
+      klo -= kofs;
+      khi -= kofs;
+      // Rows past the block (padding lanes) see Q = 0; their P and O rows are never read.
+      const bool whole = __all_sync(0xffffffffu, klo <= 0 && khi >= KH - 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / C::kSBufs) & 1, abort, p.err));
+      if (!ok) break;
+      tc_fence_after();
       if (active) {
         // (A warp without rows of the block only keeps the barrier protocol: its P and O lanes are
         // never read.)
@@ -589,12 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < KH; ++k) sv[k] = __uint_as_float(sr[k]);
         }
-        int klo = 0, khi = kChunk - 1;
-        if (rv) key_interval<RING>(p, w, t, p_i, &klo, &khi);
-        klo -= kofs;
-        khi -= kofs;
-        // Rows past the block (padding lanes) see Q = 0; their P and O rows are never read.
-        if (!__all_sync(0xffffffffu, klo <= 0 && khi >= KH - 1)) {
+        if (!whole) {
 #pragma unroll
           for (int k = 0; k < KH; ++k) sv[k] = (k >= klo && k <= khi) ? sv[k] : -INFINITY;
         }
