@@ -44,6 +44,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
 constexpr int kMmaWarp = 10;
+constexpr int kVRelayWarp = 2;    // softmax warp of TMEM lane quarter 2: tile rows 96-127
 constexpr int kGeo = 16;          // tile-geometry ring: at least the K stages plus the S buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // two O accumulators (one per warpgroup) of d columns, 128 apart
@@ -98,7 +99,7 @@ struct Bars {
   uint64_t v_empty[8];
   uint64_t geo_full[kGeo];  // tile j's geometry is in entry j % kGeo
   uint64_t s_full[3];
-  uint64_t p_full[3][2];  // [S buffer][warpgroup]
+  uint64_t p_full[3];     // [S buffer]: both warpgroups' P of the tile (every softmax thread arrives)
   uint64_t o_full[2][2];  // [warpgroup][tile parity]: one phase per P.V MMA of that parity (waited on
                           // before rescaling O_h)
   uint64_t o_done;     // one phase, after the last P.V MMA (the epilogue waits on it)
@@ -312,8 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kGeo; ++i) mbar_init(&bars->geo_full[i], 1);
     for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i][0], kSoftmaxThreads / 2);
-      mbar_init(&bars->p_full[i][1], kSoftmaxThreads / 2);
+      mbar_init(&bars->p_full[i], kSoftmaxThreads);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars->o_full[i >> 1][i & 1], 1);
     mbar_init(&bars->o_done, 1);
@@ -494,15 +494,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // O_h += P_h V_h for tile jp over the keys [h kKH, (h + 1) kKH) of warpgroup h, which has
         // zeroed the V rows of its keys that lie outside every query's range before arriving.
+        // V_jp has landed: a softmax warp waits for it before it arrives on the tile's P barrier.
         const int st = jp % C::kVStages;
-        ok = mbar_wait(&bars->v_full[st], (jp / C::kVStages) & 1, abort, p.err);
-        if (!ok) break;
         const uint64_t vd = vdesc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
         const int sb = jp % C::kSBufs;
+        // One wait for both halves: the warpgroups finish a tile's P together, and every wait
+        // costs the issuer about as much as two MMAs of the tile, with the tensor pipe idle.
+        ok = mbar_wait(&bars->p_full[sb], (jp / C::kSBufs) & 1, abort, p.err);
+        if (!ok) break;
+        tc_fence_after();
         for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait(&bars->p_full[sb][h], (jp / C::kSBufs) & 1, abort, p.err);
-          if (!ok) break;
-          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < C::kKH / 16; ++kk) {
             const uint64_t bdesc = vd + static_cast<uint64_t>(((h * C::kKH + 16 * kk) * 128) >> 4);
@@ -511,7 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bars->o_full[h][jp & 1]);
         }
-        if (!ok) break;
         mma_commit(&bars->v_empty[st]);
         if (jp == w.nt - 1) mma_commit(&bars->o_done);
       }
@@ -680,7 +680,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
       }
-      mbar_arrive(&bars->p_full[sb][wg]);
+      if (warp == kVRelayWarp) {
+        // This warp's arrival on the P barrier waits for V_j, so the issuer's one wait for P
+        // covers V too. In a block of at most 96 rows it is a warp without rows; otherwise its
+        // wait overlaps the other warps' softmax.
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bars->v_full[j % C::kVStages], (j / C::kVStages) & 1, abort, p.err));
+        if (!ok) break;
+      }
+      mbar_arrive(&bars->p_full[sb]);
     }
     // ---- epilogue: merge the two halves into the split's partial (m, l, unnormalised O) ----
     float m_w[2] = {-INFINITY, -INFINITY}, l_w[2] = {0.f, 0.f};
