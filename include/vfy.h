@@ -109,6 +109,12 @@ VFY_API unsigned long long vfy_launch_count(const vfy_ctx* ctx);
  * through the combine kernel. */
 VFY_API vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits);
 
+/* CTAs that copy each chunk in the vfy_page_in calls enqueued afterwards: 1 to 4, or 0 (the
+ * default) for 2. Tuning knob; the copy is bit-exact either way. More CTAs keep more host reads in
+ * flight, so a page-in alone finishes sooner, but beside running attention kernels the reads in
+ * flight slow those kernels down. */
+VFY_API vfy_status vfy_set_pagein_ctas(vfy_ctx* ctx, int ctas_per_chunk);
+
 /* Test of the timeout path (0, the default, turns it off). With limit_ns != 0, every CTA of
  * the attention kernels enqueued afterwards first waits on a barrier that nothing completes, for
  * limit_ns nanoseconds. That wait runs out exactly as a pipeline wait that ran out would: it sets

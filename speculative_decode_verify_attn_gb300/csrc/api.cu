@@ -29,6 +29,7 @@ struct vfy_ctx {
   int row_tiles;                 // ceil(max_queries_per_seq * G / 128)
   unsigned long long timeout_test_ns;   // see vfy_test_wait_timeout
   int stable_metadata;                // see vfy_set_stable_metadata
+  int pagein_ctas;                    // see vfy_set_pagein_ctas (0 = 2)
 };
 
 namespace {
@@ -221,6 +222,12 @@ vfy_status vfy_set_splits(vfy_ctx* ctx, int full_splits, int swa_splits) {
   return VFY_OK;
 }
 
+vfy_status vfy_set_pagein_ctas(vfy_ctx* ctx, int ctas_per_chunk) {
+  VFY_REQUIRE(ctx != nullptr && ctas_per_chunk >= 0 && ctas_per_chunk <= vfy::kMaxPageInCtas);
+  ctx->pagein_ctas = ctas_per_chunk;
+  return VFY_OK;
+}
+
 vfy_status vfy_test_wait_timeout(vfy_ctx* ctx, uint64_t limit_ns) {
   VFY_REQUIRE(ctx != nullptr);
   ctx->timeout_test_ns = limit_ns;
@@ -310,6 +317,7 @@ vfy_status vfy_page_in(vfy_ctx* ctx, const uint16_t* host_k, const uint16_t* hos
   p.k = k;
   p.chunk_elems = static_cast<long long>(ctx->cfg.num_kv_heads) * kChunk * ctx->cfg.head_dim;
   p.err = ctx->err;
+  p.parts = ctx->pagein_ctas > 0 ? ctx->pagein_ctas : 2;
   VFY_CUDA(vfy::launch_page_in(p, s));
   ++ctx->launches;
   return VFY_OK;

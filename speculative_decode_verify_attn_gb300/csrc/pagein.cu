@@ -3,12 +3,13 @@
 // 64-token chunks page to host RAM bit-exact").
 // The device reads the host store directly (zero-copy over the host link), so the (chunk, slot)
 // list can stay in device memory and the copy can live inside a captured CUDA graph. Grid:
-// x = list entry (sequence b, entry i < k), y = half of the chunk; entries past pagein_count[b]
-// return at once. Each thread keeps 2 x 2 independent 16-byte loads in flight, so 16 chunks keep
-// half a megabyte of host reads in flight. The copy is bound by the host link's latency. Measured in
-// the 40-layer pass on GB300: two CTAs per chunk page in 20 us a pass faster than one and the pass
-// gains 2-3 us; four loads in flight per thread instead of two page in faster still but slow the
-// attention kernels beside them (the pass lost 9 us).
+// x = list entry (sequence b, entry i < k), y = part of the chunk (1 to 4 CTAs per chunk, set per
+// call); entries past pagein_count[b] return at once. Each thread keeps 2 x 2 independent 16-byte
+// loads in flight. The copy is bound by the host link's latency, and host reads in flight slow the
+// attention kernels that run beside it. Measured in the 40-layer pass on GB300 against 2 CTAs per
+// chunk: 3 or 4 cost the pass 2 and 12 us; 1 for the page-ins after the first was 0.1 us/layer
+// faster on one box and 0.02 slower on another; half the loads in flight per thread made the
+// later page-ins late for their layers.
 #include "ptx.cuh"
 #include "vfy_internal.cuh"
 
@@ -16,7 +17,6 @@ namespace vfy {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kParts = 2;
 constexpr int kUnroll = 2;
 
 __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p) {
@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p)
     return;
   }
   const long long n16 = p.chunk_elems / 8;                   // 16-byte words per chunk
-  const long long per = (n16 + kParts - 1) / kParts;
+  const long long per = (n16 + gridDim.y - 1) / gridDim.y;
   const long long w0 = blockIdx.y * per;
   const long long w1 = min(n16, w0 + per);
   const uint4* sk = reinterpret_cast<const uint4*>(p.host_k + chunk * p.chunk_elems);
@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kThreads) page_in_kernel(const PageInParams p)
 }  // namespace
 
 cudaError_t launch_page_in(const PageInParams& p, cudaStream_t stream) {
-  dim3 grid(p.num_seqs * p.k, kParts);
+  if (p.parts < 1 || p.parts > kMaxPageInCtas) return cudaErrorInvalidValue;
+  dim3 grid(p.num_seqs * p.k, p.parts);
   return launch_pdl(page_in_kernel, grid, dim3(kThreads), 0, stream, p);
 }
 

@@ -52,6 +52,7 @@ struct AttnParams {
 // Splits of one (sequence, KV head) that one cluster can merge in the attention kernel (the
 // largest non-portable cluster).
 constexpr int kMaxClusterSplits = 16;
+constexpr int kMaxPageInCtas = 4;     // CTAs per chunk of a page-in
 
 struct CombineParams {
   const int32_t* cu_q;
@@ -139,6 +140,7 @@ struct PageInParams {
   int k;
   long long chunk_elems;      // Hkv * 64 * d
   int* err;
+  int parts;                  // CTAs per chunk, 1 .. kMaxPageInCtas
 };
 cudaError_t launch_page_in(const PageInParams& p, cudaStream_t stream);
 

@@ -25,6 +25,13 @@ import torch
 from . import synth, vfy
 
 CHUNK = 64
+# CTAs per chunk of the page-ins. The first full layer waits for the first page-in; the others
+# run beside the layers, whose attention kernels their host reads in flight slow down. On GB300,
+# 3 or 4 CTAs for all cost the pass 2 and 12 us; 1 for the page-ins after the first was 0.1
+# us/layer faster than 2 on one box and 0.02 slower on another (the host link differs by box),
+# so both keep 2.
+PAGEIN_CTAS_FIRST = 2
+PAGEIN_CTAS_REST = 2
 
 
 def _packed(layout, dev):
@@ -226,9 +233,11 @@ class VerifyPass:
         vfy.vfy_select_resident(self.ctx, self.scores, self.cu_chunks, 1, self.n_chunks, self.k,
                                 self.slot_of_chunk, self.res_ids, self.res_slots, self.cu_res,
                                 self.pagein_list, self.pagein_count, main)
-        for l in self.full_layers:
+        for i, l in enumerate(self.full_layers):
+            vfy.vfy_set_pagein_ctas(self.ctx, PAGEIN_CTAS_FIRST if i == 0 else PAGEIN_CTAS_REST)
             vfy.vfy_page_in(self.ctx, self.host_k[l], self.host_v[l], self.n_chunks, self.pool_k[l],
                             self.pool_v[l], self.k, self.pagein_list, self.pagein_count, 1, self.k, main)
+        vfy.vfy_set_pagein_ctas(self.ctx, 0)
 
     def enqueue_layers(self):
         """The attention layers alone, in pass order, on the current stream."""
@@ -278,13 +287,15 @@ class VerifyPass:
                 vfy.vfy_select_resident(self.ctx, self.scores, self.cu_chunks, 1, self.n_chunks, self.k,
                                         self.slot_of_chunk, self.res_ids, self.res_slots, self.cu_res,
                                         self.pagein_list, self.pagein_count, self.side)
-                for l in self.full_layers:
+                for i, l in enumerate(self.full_layers):
+                    vfy.vfy_set_pagein_ctas(self.ctx, PAGEIN_CTAS_FIRST if i == 0 else PAGEIN_CTAS_REST)
                     vfy.vfy_page_in(self.ctx, self.host_k[l], self.host_v[l], self.n_chunks, self.pool_k[l],
                                     self.pool_v[l], self.k, self.pagein_list, self.pagein_count, 1, self.k,
                                     self.side)
                     ev = torch.cuda.Event()
                     ev.record(self.side)
                     events[l] = ev
+                vfy.vfy_set_pagein_ctas(self.ctx, 0)
                 if paging_tail is not None:
                     waits["accept"] = paging_tail()
             joins = join_points(len(self.full_layers))

@@ -16,7 +16,7 @@ VFY_OK, VFY_EINVAL, VFY_ECUDA, VFY_ENOMEM, VFY_EUNSUPPORTED, VFY_EDEVICE_INPUT, 
 EXPORTS = ("vfy_create", "vfy_destroy", "vfy_get_status", "vfy_strerror", "vfy_set_splits",
            "vfy_select_resident", "vfy_page_in", "vfy_attend_full", "vfy_attend_swa", "vfy_accept",
            "vfy_accept_static", "vfy_launch_count", "vfy_append_full", "vfy_append_swa",
-           "vfy_gate_depths", "vfy_test_wait_timeout", "vfy_set_stable_metadata")
+           "vfy_gate_depths", "vfy_test_wait_timeout", "vfy_set_stable_metadata", "vfy_set_pagein_ctas")
 
 
 class VfyError(RuntimeError):
@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L.vfy_set_splits.argtypes = [_P, _I, _I]
         L.vfy_test_wait_timeout.argtypes = [_P, ctypes.c_uint64]
         L.vfy_set_stable_metadata.argtypes = [_P, _I]
+        L.vfy_set_pagein_ctas.argtypes = [_P, _I]
         L.vfy_select_resident.argtypes = [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
         L.vfy_page_in.argtypes = [_P, _P, _P, ctypes.c_int64, _P, _P, _I, _P, _P, _I, _I, _P]
         L.vfy_attend_full.argtypes = [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P]
@@ -190,6 +191,11 @@ def vfy_test_wait_timeout(ctx: Context, limit_ns: int = 0):
     """Test of the timeout path: every attention CTA enqueued afterwards first runs one wait of
     limit_ns that cannot complete (0 turns the test off). See include/vfy.h."""
     _check(lib().vfy_test_wait_timeout(ctx.handle, int(limit_ns)), "vfy_test_wait_timeout")
+
+
+def vfy_set_pagein_ctas(ctx: Context, ctas_per_chunk: int = 0):
+    """CTAs per chunk of the page-ins enqueued afterwards (1-4; 0 = 2). See include/vfy.h."""
+    _check(lib().vfy_set_pagein_ctas(ctx.handle, int(ctas_per_chunk)), "vfy_set_pagein_ctas")
 
 
 def vfy_set_stable_metadata(ctx: Context, stable: bool = True):

@@ -108,7 +108,10 @@ def test_select_rotating_schedule_pages_16(H, vfy, ctx):
         prev = check_select(H, vfy, ctx, rot.scores(step), [0, 4096], 128, prev).astype(np.int32)
 
 
-def test_page_in_bit_exact(H, vfy, ctx):
+@pytest.mark.parametrize("ctas", [0, 1, 3, 4])
+def test_page_in_bit_exact(H, vfy, ctx, ctas):
+    """Every CTAs-per-chunk setting (0 = the default 2) copies the chosen chunks bit-exactly and
+    touches no other slot."""
     rng = np.random.default_rng(5)
     n_host, n_slots, k = 40, 12, 12
     hk = rng.integers(0, 65536, (n_host, 4, 64, 128), dtype=np.uint16)
@@ -120,13 +123,24 @@ def test_page_in_bit_exact(H, vfy, ctx):
     pairs = [(3, 5), (39, 0), (7, 11), (0, 2)]
     plist = np.full((k, 2), -1, np.int32)
     plist[: len(pairs)] = pairs
-    vfy.vfy_page_in(ctx, host_k, host_v, n_host, pk, pv, n_slots, H.dev_i32(plist), H.dev_i32([len(pairs)]),
-                    1, k)
+    vfy.vfy_set_pagein_ctas(ctx, ctas)
+    try:
+        vfy.vfy_page_in(ctx, host_k, host_v, n_host, pk, pv, n_slots, H.dev_i32(plist), H.dev_i32([len(pairs)]),
+                        1, k)
+    finally:
+        vfy.vfy_set_pagein_ctas(ctx, 0)
     torch.cuda.synchronize()
     gk, gv = H.bits_of(pk), H.bits_of(pv)
     nk, nv = O.page_in(hk, hv, np.zeros_like(gk), np.zeros_like(gv), pairs)
     assert gk.tobytes() == nk.tobytes() and gv.tobytes() == nv.tobytes()
     assert vfy.vfy_get_status(ctx) == vfy.VFY_OK
+
+
+def test_page_in_ctas_bounds(vfy, ctx):
+    for bad in (-1, 5):
+        with pytest.raises(vfy.VfyError) as e:
+            vfy.vfy_set_pagein_ctas(ctx, bad)
+        assert e.value.status == vfy.VFY_EINVAL
 
 
 def test_page_in_rejects_pageable_memory(H, vfy, ctx):
