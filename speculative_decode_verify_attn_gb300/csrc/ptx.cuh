@@ -248,6 +248,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+#define VFY_R8A(i) "=r"(a[i + 0]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), "=r"(a[i + 4]), "=r"(a[i + 5]), \
+                   "=r"(a[i + 6]), "=r"(a[i + 7])
+#define VFY_R8C(i) "=r"(b[i + 0]), "=r"(b[i + 1]), "=r"(b[i + 2]), "=r"(b[i + 3]), "=r"(b[i + 4]), "=r"(b[i + 5]), \
+                   "=r"(b[i + 6]), "=r"(b[i + 7])
+// Load 32 consecutive 32-bit columns at each of two TMEM addresses (this warp's 32 lanes) and
+// wait once for both.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : VFY_R8A(0), VFY_R8A(8), VFY_R8A(16), VFY_R8A(24), VFY_R8C(0), VFY_R8C(8), VFY_R8C(16), VFY_R8C(24)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+#undef VFY_R8A
+#undef VFY_R8C
+
 #define VFY_R8B(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
                    "=r"(r[i + 6]), "=r"(r[i + 7])
 // Load 64 consecutive 32-bit columns of this warp's 32 TMEM lanes and wait.
