@@ -61,9 +61,10 @@ constexpr int kBarsBytes = 4096;  // shared memory reserved for the barrier bloc
 // rank, rank + n, ...; slot k holds row rank + n k) one fp32 (m, l) pair and one bf16 O row
 // (normalised by l) per split, at index k * n + split. k * n + split < kMaxRows + n, so
 // kMaxRows + kMaxClusterSplits entries cover every cluster size. A merging CTA processes few
-// tiles, so it takes fewer K/V stages. Forwarding the rows as bf16 halved what the merge moves:
-// window layers 7.50 -> 7.30 us in their chain (the rounding, about 2^-9 of a partial, stays far
-// inside the attention tolerance).
+// tiles, so it takes fewer K/V stages. Sending the rows as bf16 halved what the merge moves
+// (window layers 7.50 -> 7.30 us in their chain; the rounding, about 2^-9 of a partial, stays far
+// inside the attention tolerance), and sending them straight from the softmax threads' registers,
+// with no staging in shared memory and no barrier before the sends, 7.09 -> 6.68 us.
 template <int HD, bool RING, bool MERGE, bool WIDE>
 struct Cfg {
   static_assert(!WIDE || (!RING && !MERGE), "wide tiles are for full layers without the cluster merge");
@@ -271,17 +272,6 @@ __device__ __forceinline__ void key_interval(const AttnParams& p, const Work& w,
     *klo = a - shift;
     *khi = b - shift;
   }
-}
-
-// Cluster merge: a split first stages its merged O rows in its own (then idle) K/V stages, as bf16
-// normalised by the split's row sum: row r at r * HD * 2 bytes, 16-byte chunk ch at chunk
-// ch ^ (r mod (HD / 8)), so that the softmax lanes of a warp (consecutive rows) write one chunk
-// column without all landing in one bank group, and a warp reading one row sees a permutation of
-// its chunks.
-template <int HD>
-__device__ __forceinline__ uint32_t staged16_offset(int r, int ch) {
-  constexpr int kChunks = HD / 8;                      // 16-byte chunks (8 bf16) per row
-  return static_cast<uint32_t>(r * HD * 2 + ((ch ^ (r & (kChunks - 1))) << 4));
 }
 
 template <int HD, bool RING, bool MERGE, bool WIDE, bool DIRECT = false>
@@ -715,18 +705,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if constexpr (MERGE) {
-      // Stage the split's rows locally as bf16, normalised by the split's row sum l (the (m, l)
-      // pair stays fp32); a split without data for a row stages (-inf, 0) and no O. Then the
-      // softmax warps forward the rows into the receive area of each row's owner, split rank
-      // r % n: one 16-byte store per lane, 32 / (d / 8) rows per warp store.
-      uint8_t* so = sK;                                // the K and V stages, idle after o_done
+      // Each softmax thread sends its row's half of the columns, [h d/2, (h + 1) d/2) for
+      // warpgroup h, straight from registers into the receive area of the row's owner, split rank
+      // r % n: bf16 normalised by the split's row sum l, eight 16-byte stores; warpgroup 0 also
+      // sends the (m, l) pair (fp32). A split without data for a row sends (-inf, 0) and no O.
+      const int n = static_cast<int>(cluster_nctarank());
+      const int rank = static_cast<int>(cluster_ctarank());
+      const uint32_t recv = smem_u32(smem + C::kRecvOffset);
+      const uint32_t recv_ml = smem_u32(smem + C::kRecvMlOffset);
+      const unsigned rq = static_cast<unsigned>(lr) / static_cast<unsigned>(n);
+      const int e = static_cast<int>(rq) * n + rank;     // entry in the owner's receive area
+      const uint32_t owner = static_cast<uint32_t>(lr - static_cast<int>(rq) * n);
+      if (rv && wg == 0)
+        st_dsmem_f2(dsmem_addr(recv_ml + e * 8, owner), make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum));
       if (ok && w.nt > 0) {
         const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        const uint32_t row_at = recv + e * HD * 2 + wg * HD;   // this half's bytes of the entry
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
           uint32_t o0[32], o1[32];
-          // both halves' columns with one wait (in the narrow kernel's partial epilogue the same
-          // change measured 0.17 us slower per full layer, so that one keeps two)
           tmem_ld32x2(lane_base + kColO + wg * (HD / 2) + c * 32, lane_base + kColO + 128 + wg * (HD / 2) + c * 32,
                       o0, o1);
           if (rv && l_sum > 0.f) {
@@ -734,39 +731,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 0; x < 32; x += 8) {
               uint32_t pk[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float a = (w0 * __uint_as_float(o0[x + 2 * e]) + w1 * __uint_as_float(o1[x + 2 * e])) * inv;
+              for (int q = 0; q < 4; ++q) {
+                const float a = (w0 * __uint_as_float(o0[x + 2 * q]) + w1 * __uint_as_float(o1[x + 2 * q])) * inv;
                 const float b =
-                    (w0 * __uint_as_float(o0[x + 2 * e + 1]) + w1 * __uint_as_float(o1[x + 2 * e + 1])) * inv;
+                    (w0 * __uint_as_float(o0[x + 2 * q + 1]) + w1 * __uint_as_float(o1[x + 2 * q + 1])) * inv;
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-                pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                pk[q] = *reinterpret_cast<const uint32_t*>(&h2);
               }
-              *reinterpret_cast<uint4*>(so + staged16_offset<HD>(lr, (wg * (HD / 2) + c * 32 + x) >> 3)) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              st_dsmem_u4(dsmem_addr(row_at + (c * 32 + x) * 2, owner), make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
           }
-        }
-      }
-      if (wg == 0) bars->sml[lr] = make_float2(l_sum > 0.f ? m_row : -INFINITY, l_sum);
-      named_bar_sync(1, kSoftmaxThreads);
-      const int n = static_cast<int>(cluster_nctarank());
-      const int rank = static_cast<int>(cluster_ctarank());
-      constexpr int kChunks = HD / 8;                  // 16-byte chunks per row
-      constexpr int kRowsPerStore = 32 / kChunks;      // rows one warp store forwards
-      const int sub = lane / kChunks, ch = lane % kChunks;
-      const uint32_t recv = smem_u32(smem + C::kRecvOffset);
-      const uint32_t recv_ml = smem_u32(smem + C::kRecvMlOffset);
-      for (int rb = warp * kRowsPerStore; rb < w.rows; rb += (kSoftmaxThreads / 32) * kRowsPerStore) {
-        const int rr = rb + sub;
-        if (rr < w.rows) {
-          const float2 ml = bars->sml[rr];
-          const unsigned rq = static_cast<unsigned>(rr) / static_cast<unsigned>(n);
-          const int e = static_cast<int>(rq) * n + rank;  // entry in the owner's receive area
-          const uint32_t owner = static_cast<uint32_t>(rr - static_cast<int>(rq) * n);
-          if (ch == 0) st_dsmem_f2(dsmem_addr(recv_ml + e * 8, owner), ml);
-          if (ml.y > 0.f)
-            st_dsmem_u4(dsmem_addr(recv + e * HD * 2 + ch * 16, owner),
-                        *reinterpret_cast<const uint4*>(so + staged16_offset<HD>(rr, ch)));
         }
       }
     } else if constexpr (DIRECT) {
