@@ -1,6 +1,7 @@
 // Verify attention on sm_103a: split-KV flash-decode with TMA-staged bf16 K/V tiles, tcgen05
 // tensor-core tiles for S = Q K^T and O += P V (fp32 accumulators in tensor memory), an fp32
-// online softmax, and a warp-shuffle combine of the splits.
+// online softmax, and the splits merged either in a thread-block cluster (distributed shared
+// memory) or by a combine kernel.
 //
 // Sources ("Laguna XS 2.1 33B on a RTX 3090" (lucebox)):
 //  - "The model, fast MoE with a drafter in the box": the 16 drafted tokens and the last committed
@@ -17,8 +18,9 @@
 //              half of every tile's keys and keeps its own running maximum, row sum and O
 //              accumulator (O_h += P_h V_h), so the two halves never wait on each other; they are
 //              merged once, in the epilogue. A tile is two 64-token chunks (one per warpgroup) in
-//              full layers and one chunk (32 keys per warpgroup) in window layers and in merging
-//              launches, which are latency-bound.
+//              full layers whose splits hold at least 8 chunks, and one chunk (32 keys per
+//              warpgroup) otherwise: short splits and merging launches are latency-bound. Warp 2
+//              also relays each tile's V to the issuer through its arrival on the tile's P barrier.
 //   warp 8     TMA producer of K tiles (a ring of smem stages, released when S has read them) and
 //              of the tile geometry the softmax needs (a ring of its own)
 //   warp 9     TMA producer of V tiles (a ring released when P.V has read them)
