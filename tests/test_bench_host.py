@@ -94,3 +94,11 @@ def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     src.write_bytes(b"kernel v2")
     assert bench.profiled_traffic("p.md", "attend.cu") is None
     assert bench.profiled_traffic("missing.md", "attend.cu") is None
+
+
+def test_committed_profiles_match_the_kernel_sources():
+    """The committed ncu summaries the bench line takes `traffic` from were captured on the
+    kernel sources as they stand: a kernel changed without a new capture reports no traffic."""
+    assert bench.profiled_traffic("attend_swa_window512.md", "attend.cu") is not None
+    assert bench.profiled_traffic("attend_full_8k_resident.md", "attend.cu") is not None
+    assert bench.profiled_traffic("accept_17x131072.md", "accept.cu") is not None
